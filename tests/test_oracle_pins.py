@@ -1,0 +1,370 @@
+"""Pins for the CPU oracle against facts fixed outside the oracle itself.
+
+Each test checks the oracle against the pages' identity and examples,
+closed forms, exact rational arithmetic or a library routine the oracle
+does not use, so that a dropped term, a wrong sign or index, or a
+transposed operand in the oracle fails one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction as Fr
+
+import numpy as np
+import pytest
+
+from oracle import sq_oracle as O
+from w8a8_post_quantization_02_b300 import synth
+
+F32 = np.float32
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- exact helpers
+def rn_bin(v: Fr, p: int, emin: int = -126) -> Fr:
+    """Round a rational to a binary format with a p-bit significand (RNE)."""
+    if v == 0:
+        return Fr(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fr(2) ** e > a:
+        e -= 1
+    elif Fr(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, emin)
+    ulp = Fr(2) ** (e - (p - 1))
+    r = round(a / ulp) * ulp  # Fraction.__round__ is half-to-even
+    return r if v > 0 else -r
+
+
+def rn32(v: Fr) -> Fr:
+    return rn_bin(v, 24)
+
+
+def rn_sqrt32(a: Fr) -> Fr:
+    """Correctly rounded binary32 sqrt by exact comparison with midpoints."""
+    f = F32(math.sqrt(float(a)))
+    for _ in range(4):
+        lo, hi = np.nextafter(f, F32(0)), np.nextafter(f, F32(np.inf))
+        m_lo = (Fr(float(lo)) + Fr(float(f))) / 2
+        m_hi = (Fr(float(f)) + Fr(float(hi))) / 2
+        if m_lo * m_lo > a:
+            f = lo
+        elif m_hi * m_hi < a:
+            f = hi
+        else:
+            return Fr(float(f))
+    raise AssertionError("sqrt candidate search did not settle")
+
+
+def bf16_from_fraction(v: Fr) -> int:
+    r = rn_bin(v, 8)
+    f = F32(float(r))
+    return int(f.view(np.uint32) >> 16)
+
+
+def brute_path(x, w, alpha_kind):
+    """Independent exact-rational restatement of steps 1-5 on tiny inputs."""
+    T, K = x.shape
+    N = w.shape[1]
+    X = [[Fr(float(v)) for v in row] for row in x]
+    W = [[Fr(float(v)) for v in row] for row in w]
+    amax_x = [max(abs(X[t][j]) for t in range(T)) for j in range(K)]
+    amax_w = [max(abs(W[j][n]) for n in range(N)) for j in range(K)]
+    floor = Fr(float(F32(1e-5)))
+    smin, smax = floor, Fr(float(F32(1e5)))
+    s = []
+    for j in range(K):
+        ax, aw = max(amax_x[j], floor), max(amax_w[j], floor)
+        if alpha_kind == "half":
+            p, q = rn_sqrt32(ax), rn_sqrt32(aw)
+        elif alpha_kind == "one":
+            p, q = ax, Fr(1)
+        else:  # "zero"
+            p, q = Fr(1), aw
+        s.append(min(max(rn32(p / q), smin), smax))
+    s_inv = [rn32(1 / sj) for sj in s]
+
+    def quant(vals):
+        amax = max(abs(v) for v in vals)
+        d = Fr(1) if amax == 0 else rn32(amax / 127)
+        inv = rn32(1 / d)
+        codes = [max(-127, min(127, round(rn32(v * inv)))) for v in vals]
+        return codes, d
+
+    wf = [[rn32(s[j] * W[j][n]) for n in range(N)] for j in range(K)]
+    wq, wsc = [], []
+    for n in range(N):
+        c, d = quant([wf[j][n] for j in range(K)])
+        wq.append(c)
+        wsc.append(d)
+    xq, xsc = [], []
+    for t in range(T):
+        c, d = quant([rn32(X[t][j] * s_inv[j]) for j in range(K)])
+        xq.append(c)
+        xsc.append(d)
+    acc = [[sum(xq[t][j] * wq[n][j] for j in range(K)) for n in range(N)] for t in range(T)]
+    y = [[bf16_from_fraction(acc[t][n] * xsc[t] * wsc[n]) for n in range(N)] for t in range(T)]
+    return dict(amax_x=amax_x, amax_w=amax_w, s=s, s_inv=s_inv, wq=wq, w_scale=wsc,
+                xq=xq, x_scale=xsc, acc=acc, y=y)
+
+
+def _f(a):
+    return [Fr(float(v)) for v in np.asarray(a).ravel()]
+
+
+# ---------------------------------------------------------------- identity / orientation
+def _small_case(seed=0, T=48, K=96, N=96, alpha=0.5, dtype="f32"):
+    return synth.make_case("pin", T, K, N, dtype=dtype, alpha=alpha, outlier_frac=0.05,
+                           outlier_lo=20.0, outlier_hi=100.0, seed=seed)
+
+
+@pytest.mark.parametrize("alpha", [0.5, 0.85])
+def test_identity_unquantized_rewrite(alpha):
+    """(X S^-1)(S W) == X W to <= 1e-5 relative in float64, using the oracle's
+    own binary32 X' and W' (first page, paragraph 1)."""
+    c = _small_case(alpha=alpha)
+    x, w = c.x_f32().astype(np.float64), c.w_f32().astype(np.float64)
+    ax, aw = O.calibrate_absmax(c.x_f32(), 0), O.calibrate_absmax(c.w_f32(), 1)
+    s, s_inv, nf = O.smooth_factors(ax, aw, alpha)
+    assert not nf
+    _, _, _, wf = O.fold_quantize_weight(c.w_f32(), s, return_folded=True)
+    _, _, _, xs = O.quant_act(c.x_f32(), s_inv, return_scaled=True)
+    y = x @ w
+    y2 = xs.astype(np.float64) @ wf.astype(np.float64)
+    rel = np.linalg.norm(y2 - y) / np.linalg.norm(y)
+    assert rel <= 1e-5
+    # the exact-arithmetic version of the same identity with the oracle's s
+    s64 = s.astype(np.float64)
+    rel_exact = np.linalg.norm((x / s64) @ (s64[:, None] * w) - y) / np.linalg.norm(y)
+    assert rel_exact <= 1e-12
+
+
+def test_wrong_dimension_is_a_different_map():
+    """Scaling W's columns instead of its rows breaks the identity (first page, paragraph 1)."""
+    c = _small_case(K=96, N=96)
+    x, w = c.x_f32().astype(np.float64), c.w_f32().astype(np.float64)
+    s, _, _ = O.smooth_factors(O.calibrate_absmax(c.x_f32(), 0),
+                               O.calibrate_absmax(c.w_f32(), 1), 0.5)
+    s64 = s.astype(np.float64)
+    y = x @ w
+    wrong = (x / s64) @ (w * s64[None, :])
+    assert np.linalg.norm(wrong - y) / np.linalg.norm(y) > 1e-2
+    # and the oracle's fold really scales rows: W'[j, :] == RN32(s_j * W[j, :])
+    _, _, _, wf = O.fold_quantize_weight(c.w_f32(), s, return_folded=True)
+    j = int(np.argmax(s))
+    assert np.array_equal(wf[j], (s[j] * c.w_f32()[j]).astype(F32))
+    assert not np.array_equal(wf[:, j], (s[j] * c.w_f32()[:, j]).astype(F32))
+
+
+def test_matrix_lab_example():
+    """diag(0.25, 1): determinant 0.25, e1 -> e1/4, e2 fixed, weight row 0 x4."""
+    g = json.load(open(os.path.join(GOLDEN, "matrix_lab.json")))
+    # statistics chosen so that alpha = 0.5 gives s = (4, 1)
+    s, s_inv, nf = O.smooth_factors(np.array([16.0, 1.0], F32), np.array([1.0, 1.0], F32), 0.5)
+    assert not nf
+    assert s.tolist() == g["compensating_weight_scale"]
+    m = np.diag(s_inv.astype(np.float64))
+    assert m.tolist() == g["matrix"]
+    assert np.linalg.det(m) == pytest.approx(g["determinant"], abs=0)
+    _, _, _, xs = O.quant_act(np.eye(2, dtype=F32), s_inv, return_scaled=True)
+    assert xs[0].tolist() == g["image_e1"] and xs[1].tolist() == g["image_e2"]
+    w = np.array([[0.5, -1.0, 2.0], [3.0, 0.25, -0.75]], F32)
+    _, _, _, wf = O.fold_quantize_weight(w, s, return_folded=True)
+    assert wf[0].tolist() == (4 * w[0]).tolist() and wf[1].tolist() == w[1].tolist()
+
+
+def test_lone_outlier_becomes_geometric_mean():
+    """alpha = 0.5: a lone spike o in channel j becomes sqrt(|o| max|W_j|)
+    (Smooth Rotation review, key_machinery and load_bearing_attack)."""
+    rng_x = synth.normal(3, 1, 32 * 64, 0.01).reshape(32, 64).astype(F32)
+    w = synth.normal(3, 2, 64 * 48, 0.02).reshape(64, 48).astype(F32)
+    j, t, o = 17, 5, F32(-750.0)
+    rng_x[t, j] = o
+    ax, aw = O.calibrate_absmax(rng_x, 0), O.calibrate_absmax(w, 1)
+    s, s_inv, _ = O.smooth_factors(ax, aw, 0.5)
+    _, _, _, xs = O.quant_act(rng_x, s_inv, return_scaled=True)
+    want = math.sqrt(abs(float(o)) * float(aw[j]))
+    got = float(np.max(np.abs(xs[:, j])))
+    assert abs(got - want) <= 4 * float(np.spacing(F32(want)))
+    # the weight row grows by the same factor: max|W'_j| = sqrt(|o| max|W_j|) as well
+    _, _, _, wf = O.fold_quantize_weight(w, s, return_folded=True)
+    assert abs(float(np.max(np.abs(wf[j]))) - want) <= 4 * float(np.spacing(F32(want)))
+
+
+# ---------------------------------------------------------------- brute force
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("alpha_kind,alpha", [("half", 0.5), ("one", 1.0), ("zero", 0.0)])
+def test_brute_force_tiny(seed, alpha_kind, alpha):
+    T, K, N = 1 + seed % 4, 2 + (3 * seed) % 7, 1 + (5 * seed) % 4
+    x = synth.normal(seed, 11, T * K, 1.0).reshape(T, K).astype(F32)
+    w = synth.normal(seed, 12, K * N, 0.02).reshape(K, N).astype(F32)
+    if seed % 3 == 0:
+        x[:, 0] *= F32(60.0)
+    if seed == 4:
+        x[0, :] = 0.0  # an all-zero token
+        w[:, 0] = 0.0  # an all-zero output channel
+    ref = brute_path(x, w, alpha_kind)
+    got = O.run_path(x, w, alpha)
+    assert _f(got["amax_x"]) == ref["amax_x"]
+    assert _f(got["amax_w"]) == ref["amax_w"]
+    assert _f(got["s"]) == ref["s"]
+    assert _f(got["s_inv"]) == ref["s_inv"]
+    assert got["wq"].tolist() == ref["wq"]
+    assert _f(got["w_scale"]) == ref["w_scale"]
+    assert got["xq"].tolist() == ref["xq"]
+    assert _f(got["x_scale"]) == ref["x_scale"]
+    assert got["acc"].tolist() == ref["acc"]
+    assert got["y"].tolist() == ref["y"]
+
+
+# ---------------------------------------------------------------- closed forms
+def test_calibrate_matches_loops():
+    a = synth.normal(1, 1, 37 * 53, 1.0).reshape(37, 53).astype(F32)
+    a[3, 4] = -9.0
+    col = [max(abs(float(a[t, j])) for t in range(37)) for j in range(53)]
+    row = [max(abs(float(a[t, j])) for j in range(53)) for t in range(37)]
+    assert O.calibrate_absmax(a, 0).tolist() == col
+    assert O.calibrate_absmax(a, 1).tolist() == row
+    prev = np.full(53, 2.5, F32)
+    assert O.calibrate_absmax(a, 0, prev).tolist() == [max(2.5, v) for v in col]
+    b = a.copy()
+    b[7, 9] = np.nan
+    assert np.isnan(O.calibrate_absmax(b, 0)[9]) and np.isnan(O.calibrate_absmax(b, 1)[7])
+
+
+def test_rne_ties_and_clamp():
+    # s = 1, row absmax 127 -> scale 1 and codes are rne(x) exactly
+    x = np.array([[2.5, 3.5, -2.5, 0.5, 1.5, -127.0, 127.0, 126.5, -0.5]], F32)
+    q, d, nf = O.quant_act(x, np.ones(x.shape[1], F32))
+    assert d.tolist() == [1.0] and not nf
+    assert q.tolist() == [[2, 4, -2, 0, 2, -127, 127, 126, 0]]
+
+
+def test_absmax_element_maps_to_127():
+    c = _small_case(seed=5)
+    s, s_inv, _ = O.smooth_factors(O.calibrate_absmax(c.x_f32(), 0),
+                                   O.calibrate_absmax(c.w_f32(), 1), 0.5)
+    xq, _, _, xs = O.quant_act(c.x_f32(), s_inv, return_scaled=True)
+    arg = np.argmax(np.abs(xs), axis=1)
+    assert np.array_equal(np.abs(xq[np.arange(xq.shape[0]), arg]), np.full(xq.shape[0], 127))
+    wq, _, _, wf = O.fold_quantize_weight(c.w_f32(), s, return_folded=True)
+    argw = np.argmax(np.abs(wf), axis=0)
+    assert np.array_equal(np.abs(wq[np.arange(wq.shape[0]), argw]), np.full(wq.shape[0], 127))
+    assert xq.min() >= -127 and wq.min() >= -127
+
+
+def test_zero_rows_and_columns():
+    x = np.zeros((3, 8), F32)
+    x[1] = np.arange(8, dtype=F32) - 3
+    q, d, _ = O.quant_act(x, np.ones(8, F32))
+    assert d[0] == 1.0 and d[2] == 1.0 and (q[0] == 0).all() and (q[2] == 0).all()
+    w = np.ones((8, 4), F32)
+    w[:, 2] = 0
+    wq, ws, _ = O.fold_quantize_weight(w, np.ones(8, F32))
+    assert ws[2] == 1.0 and (wq[2] == 0).all() and (wq[0] == 127).all()
+    # a zero statistic is floored, giving a finite nonzero factor
+    s, s_inv, nf = O.smooth_factors(np.array([0.0], F32), np.array([0.0], F32), 0.5)
+    assert not nf and s[0] == 1.0 and s_inv[0] == 1.0
+
+
+def test_nonfinite_statistics_flagged():
+    s, _, nf = O.smooth_factors(np.array([np.nan, 2.0], F32), np.array([1.0, np.inf], F32), 0.5)
+    assert nf and s.tolist() == [1.0, 1.0]
+    _, _, nfx = O.quant_act(np.array([[np.inf, 1.0]], F32), np.ones(2, F32))
+    assert nfx
+
+
+def test_factor_clamp_range():
+    s, _, _ = O.smooth_factors(np.array([1e30], F32), np.array([1e-30], F32), 1.0)
+    assert s[0] == F32(1e5)
+    s, _, _ = O.smooth_factors(np.array([1e-30], F32), np.array([1e30], F32), 0.0)
+    assert s[0] == F32(1e-5)
+
+
+@pytest.mark.parametrize("x,y,want", [
+    (16.0, 0.5, 4.0), (4.0, 0.5, 2.0), (0.25, 0.5, 0.5), (16.0, 0.75, 8.0),
+    (2.0 ** 20, 0.25, 32.0), (5.0, 1.0, 5.0), (5.0, 0.0, 1.0), (2.0 ** -20, 0.5, 2.0 ** -10)])
+def test_pow_exact_cases(x, y, want):
+    assert O.rn32_pow(x, y) == F32(want)
+
+
+def test_pow_half_is_correctly_rounded_sqrt():
+    xs = np.abs(synth.normal(7, 1, 400, 30.0)).astype(F32) + F32(1e-3)
+    for x in xs:
+        assert O.rn32_pow(x, 0.5) == np.sqrt(F32(x))  # IEEE sqrt is correctly rounded
+
+
+def test_pow_matches_libm_double_away_from_midpoints():
+    """The float64 libm pow decides the binary32 rounding whenever it is far
+    (relative 1e-14) from a binary32 midpoint; the oracle must agree."""
+    xs = np.concatenate([np.abs(synth.normal(9, 1, 300, 50.0)),
+                         np.abs(synth.normal(9, 2, 100, 0.02))]).astype(F32) + F32(1e-4)
+    checked = 0
+    for y in (0.85, 0.15, 0.8, 0.2, 0.3, 0.7, 0.65):
+        yf = F32(y)
+        for x in xs:
+            d = math.pow(float(x), float(yf))
+            f = F32(d)
+            lo, hi = np.nextafter(f, F32(0)), np.nextafter(f, F32(np.inf))
+            m_lo, m_hi = (float(lo) + float(f)) / 2, (float(f) + float(hi)) / 2
+            if not (m_lo * (1 + 1e-14) < d < m_hi * (1 - 1e-14)):
+                continue
+            assert O.rn32_pow(x, yf) == f
+            checked += 1
+    assert checked > 2700
+
+
+def test_smoothing_formula_general_alpha():
+    """s = x^a / w^(1-a) with a binary32 quotient of the two powers."""
+    ax = np.array([3.0, 120.0, 0.5], F32)
+    aw = np.array([0.05, 0.02, 0.1], F32)
+    s, s_inv, _ = O.smooth_factors(ax, aw, 0.85)
+    for j in range(3):
+        p = F32(math.pow(float(ax[j]), float(F32(0.85))))
+        q = F32(math.pow(float(aw[j]), float(F32(F32(1) - F32(0.85)))))
+        assert s[j] == F32(p / q)
+        assert s_inv[j] == F32(F32(1) / s[j])
+
+
+# ---------------------------------------------------------------- GEMM + epilogue
+def test_gemm_accumulators_exact():
+    rng = np.random.default_rng(0)
+    xq = rng.integers(-127, 128, size=(9, 200), dtype=np.int64).astype(np.int8)
+    wq = rng.integers(-127, 128, size=(7, 200), dtype=np.int64).astype(np.int8)
+    want = xq.astype(np.int64) @ wq.astype(np.int64).T  # integer matmul
+    assert np.array_equal(O.int_accumulate(xq, wq), want)
+    # the largest magnitude the widest layer can reach (all +-127, K = 11008)
+    k = 11008
+    a = np.full((2, k), 127, np.int8)
+    a[1] = -127
+    b = np.full((3, k), 127, np.int8)
+    acc = O.int_accumulate(a, b)
+    assert acc[0, 0] == 127 * 127 * k and acc[1, 2] == -127 * 127 * k
+
+
+def test_epilogue_rounding():
+    xq = np.array([[1], [1], [1], [3]], np.int8)
+    wq = np.array([[1]], np.int8)
+    xs = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 0.5], F32)
+    acc, y = O.w8a8_gemm(xq, xs, wq, np.array([1.0], F32))
+    assert y[:, 0].tolist() == [0x3F80, 0x3F80, 0x3F82, 0x3FC0]
+    for t in range(4):
+        assert y[t, 0] == bf16_from_fraction(Fr(int(acc[t, 0])) * Fr(float(xs[t])))
+
+
+def test_bf16_rounding_matches_exact_rationals():
+    v = np.concatenate([synth.normal(2, 3, 2000, 1.0), synth.normal(2, 4, 200, 1e-30),
+                        [0.0, -0.0, 1e-39, -3e-40, 2.0 ** -133]])
+    bits = O.bf16_rne_bits(v)
+    for a, b in zip(v, bits):
+        want = bf16_from_fraction(Fr(float(a)))
+        if a < 0 or (a == 0 and math.copysign(1, a) < 0):
+            want |= 0x8000
+        assert int(b) == want, (a, hex(int(b)), hex(want))
+
+
+def test_ulp_distance_helper():
+    a = np.array([0x3F80, 0x3F80, 0x8001, 0x0000], np.uint16)
+    b = np.array([0x3F81, 0x3F80, 0x0001, 0x8000], np.uint16)
+    assert O.bf16_ulp_distance(a, b).tolist() == [1, 0, 2, 0]
