@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Benchmark of the SmoothQuant W8A8 linear-layer hot path on B300.
+
+One step = the whole path over one layer's synthetic inputs: per-channel
+absmax of X and W, smoothing factors, fold + INT8 quantization of W, fused
+X*S^-1 + per-token INT8 quantization, and the INT8 GEMM with its bf16
+epilogue.  Inputs are resident in HBM before the timed region; L2 is
+flushed (a 256 MiB write, outside the per-step events) before every step.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.  Under torchrun each rank
+runs an independent replica (the path needs no exchange between ranks in
+this build); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W8A8 GEMM TOPS (% int8 tensor peak); act-quant GB/s (% HBM peak)"
+DEFAULT_WORKLOAD = "prefill_upgate_2048x4096x11008"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("SQ_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="sq_clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, v in enumerate(flags)
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- the oracle arm
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:  # pragma: no cover
+        return 1
+
+
+def oracle_sample_case(case, tokens: int):
+    from w8a8_post_quantization_02_b300 import synth
+    x = case.x[:tokens]
+    return synth.Case(name=case.name + f"[:{tokens}]", dtype=case.dtype, tokens=tokens, cin=case.cin,
+                      cout=case.cout, alpha=case.alpha, x=x, w=case.w, splits=case.splits)
+
+
+def time_oracle(case, budget_s: float, sample_tokens: int, max_steps: int):
+    """Run the oracle's whole path on a token sample of the layer (full W)
+    until ``max_steps`` runs or ``budget_s`` seconds are used."""
+    from oracle import sq_oracle as O
+    sc = oracle_sample_case(case, sample_tokens)
+    x, w = sc.x_f32(), sc.w_f32()
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_steps:
+        t0 = time.perf_counter()
+        O.run_path(x, w, sc.alpha)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    ops = 2 * sample_tokens * case.cin * case.cout
+    return times, ops
+
+
+def run_reference(args, case_name):
+    from w8a8_post_quantization_02_b300 import synth
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return 0
+    case = synth.workload(case_name)
+    sample_tokens = min(case.tokens, 256)
+    # warm-up runs (untimed), then the timed steps within a few minutes
+    time_oracle(case, 0.0, sample_tokens, max(1, min(args.warmup, 1)))
+    times, ops = time_oracle(case, 150.0, sample_tokens, args.steps)
+    sec = sum(times)
+    value = ops * len(times) / sec / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": sec / len(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(case, "oracle"),
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"whole path on the first {sample_tokens} tokens with the full "
+                                   f"{case.cin}x{case.cout} weight, {len(times)} runs"},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(case, codes):
+    return {"workload": case.name, "tokens": case.tokens, "cin": case.cin, "cout": case.cout,
+            "alpha": case.alpha, "input_dtype": case.dtype, "codes": codes,
+            "splits": list(case.splits) or None,
+            "l2": "flushed before every step (256 MiB write outside the step events)"}
+
+
+# ----------------------------------------------------------------- our arm
+def to_device(case, torch):
+    def conv(a):
+        if case.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a))
+    return conv(case.x), conv(case.w)
+
+
+def run_ours(args, case_name):
+    import torch
+    from w8a8_post_quantization_02_b300 import pipeline, sq, synth
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    sq.check_device(local)
+    peaks, peaks_kind = load_peaks()
+    case = synth.workload(case_name)
+    x_host, w_host = to_device(case, torch)
+    layer = pipeline.Layer.for_case(case)
+    layer.load(x_host.cuda(), w_host.cuda())
+    stream = torch.cuda.current_stream()
+    st = sq._stream(stream)
+    stages = layer.stages()
+    names = [s[0] for s in stages]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def one_step(evs=None):
+        flush.zero_()
+        if evs is not None:
+            evs[0].record(stream)
+        for i, (_, _, fn) in enumerate(stages):
+            fn(st)
+            if evs is not None:
+                evs[i + 1].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        one_step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    per_stage = np.zeros(len(stages))
+    step_ms = np.zeros(K)
+    for i in range(K):
+        for j in range(len(stages)):
+            per_stage[j] += evs[i][j].elapsed_time(evs[i][j + 1])
+        step_ms[i] = evs[i][0].elapsed_time(evs[i][-1])
+    total_ms = max_over_ranks(float(step_ms.sum()), world)
+    ops = layer.gemm_ops()
+    value = world * K * ops / (total_ms * 1e-3) / 1e12
+    stage_us = {n: per_stage[j] / K * 1e3 for j, n in enumerate(names)}
+    nbytes = layer.algorithmic_bytes()
+    hbm = float(peaks["hbm_gbs"])
+    bf16_peak = float(peaks["bf16_tflops"])
+    gemm_tops = ops / (stage_us["gemm"] * 1e-6) / 1e12
+    detail = {}
+    for n in names:
+        gbs = nbytes[n] / (stage_us[n] * 1e-6) / 1e9
+        detail[n] = {"us": round(stage_us[n], 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
+    detail["gemm"]["tops"] = round(gemm_tops, 2)
+    launches = sum(s[1] for s in stages) * K
+    tensor_path = layer.codes == "bf16"
+    if tensor_path:
+        roofline = {"bound": "tensor", "achieved": gemm_tops, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": gemm_tops / bf16_peak, "traffic": None, "kernel": "sq_w8a8_gemm (tcgen05, bf16-coded int8)",
+                    "peak_source": f"bf16 dense, {peaks_kind}"}
+    else:
+        gbs = nbytes["gemm"] / (stage_us["gemm"] * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": None, "kernel": "sq_w8a8_gemm (mma.sync s8)",
+                    "peak_source": f"HBM copy, {peaks_kind}"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+        "config": workload_config(case, layer.codes),
+        "gemm_tops": gemm_tops,
+        "act_quant_gbs": detail["quant_act"]["gbs"],
+        "act_quant_hbm_frac": detail["quant_act"]["hbm_frac"],
+        "stages": detail,
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "parallelism": f"replicas x{world}",
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(layer, stages, x_host, w_host, args.e2e_steps, ops, world, torch)
+    if rank == 0 and not args.no_cpu_baseline:
+        times, o_ops = time_oracle(case, 20.0, min(case.tokens, 256), 3)
+        line["cpu_baseline"] = {"value": o_ops * len(times) / sum(times) / 1e12, "unit": "TOPS",
+                                "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"whole path on the first {min(case.tokens, 256)} tokens with "
+                                          f"the full {case.cin}x{case.cout} weight, {len(times)} runs"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(layer, stages, x_host, w_host, steps, ops, world, torch):
+    """Same metric through the public API with host buffers: pinned-host
+    H2D of X and W, the whole path, and D2H of Y, every step."""
+    from w8a8_post_quantization_02_b300 import sq
+    xh, wh = x_host.pin_memory(), w_host.pin_memory()
+    yh = torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    st = sq._stream(stream)
+
+    def step():
+        layer.x.copy_(xh, non_blocking=True)
+        layer.w.copy_(wh, non_blocking=True)
+        for _, _, fn in stages:
+            fn(st)
+        yh.copy_(layer.y, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    return {"value": world * steps * ops / (ms * 1e-3) / 1e12, "unit": "TOPS",
+            "h2d_bytes_per_step": xh.numel() * xh.element_size() + wh.numel() * wh.element_size(),
+            "d2h_bytes_per_step": yh.numel() * yh.element_size()}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args, args.workload)
+    return run_ours(args, args.workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

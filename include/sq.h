@@ -1,0 +1,199 @@
+/*
+ * sq.h - C ABI of the B300 (sm_103a) SmoothQuant W8A8 linear-layer path.
+ *
+ * The path has five steps; each has one entry point below:
+ *
+ *   1. sq_calibrate_absmax      per-channel max|.| of X and of W
+ *   2. sq_smooth_factors        s_j = max|X_j|^a / max|W_j|^(1-a), and 1/s_j
+ *   3. sq_fold_quantize_weight  W' = diag(s) W, per-output-channel INT8 codes
+ *   4. sq_quant_act             X' = X diag(s)^-1, per-token INT8 codes
+ *   5. sq_w8a8_gemm             exact INT8 x INT8 accumulation, bf16 epilogue
+ *
+ * Orientation (first source page, "Move activation scale without changing
+ * the real linear map", paragraph 1): X is [tokens x Cin] and W is
+ * [Cin x Cout], so Y = X W; diag(s) multiplies W on its rows (input
+ * channels) and diag(s)^-1 multiplies X on its columns.
+ *
+ * Conventions for every entry point
+ *   - Pointers named dev_* or documented as "device" are CUDA device
+ *     pointers; all others are host values.  The caller allocates and owns
+ *     every buffer (inputs, outputs, workspace).  The library allocates no
+ *     memory and keeps no state between calls.
+ *   - All work is enqueued on `stream` and returns before it finishes.
+ *     Two calls on different streams may run concurrently if their
+ *     buffers do not overlap.
+ *   - Argument errors are reported synchronously by the return value and
+ *     nothing is enqueued.  A failed launch returns SQ_ERR_CUDA.
+ *   - Data-dependent conditions found on the device are OR-ed into the
+ *     optional device word `dev_flags` (SQ_FLAG_*), which the caller zeroes
+ *     and reads back when it wants them.  Kernels never trap.
+ *   - Row-major matrices take a leading dimension `ld` in elements.  The
+ *     kernels move 16-byte vectors: code buffers, and X in step 4, must be
+ *     16-byte aligned with rows a multiple of 16 bytes.  The inputs of steps
+ *     1 and 3 need only element alignment (rows that are not 16-byte
+ *     aligned take a slower element-wise path).
+ *   - The library targets sm_103a only; on any other device the launches
+ *     fail with SQ_ERR_CUDA.
+ */
+#ifndef SQ_B300_H
+#define SQ_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SQ_OK = 0,
+  SQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, alignment or enum */
+  SQ_ERR_NONFINITE = 2,    /* reserved for host-side checks of host data */
+  SQ_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+  SQ_ERR_UNSUPPORTED = 4,  /* valid request this build does not implement */
+  SQ_ERR_WORKSPACE = 5     /* workspace pointer missing or too small */
+} sq_status;
+
+/* Bits OR-ed into *dev_flags by the kernels. */
+#define SQ_FLAG_NONFINITE 0x1 /* a NaN/Inf statistic or scale was seen */
+#define SQ_FLAG_TIMEOUT 0x2   /* a bounded pipeline wait ran out */
+
+/* Element type of the floating-point inputs X and W. */
+typedef enum { SQ_F32 = 0, SQ_BF16 = 1 } sq_dtype;
+
+/* Storage of INT8 codes.  SQ_CODES_I8 stores each code as int8_t.
+ * SQ_CODES_BF16 stores the same integer (-127..127) as an exact bfloat16
+ * value; it is the operand format of the sm_103a tensor-core GEMM, since
+ * sm_103a's tcgen05.mma has no integer kind.  Both hold identical codes. */
+typedef enum { SQ_CODES_I8 = 0, SQ_CODES_BF16 = 1 } sq_codes;
+
+/* Operation ids for sq_workspace_bytes. */
+typedef enum {
+  SQ_OP_CALIBRATE = 0,
+  SQ_OP_SMOOTH = 1,
+  SQ_OP_FOLD_QUANTIZE = 2,
+  SQ_OP_QUANT_ACT = 3,
+  SQ_OP_GEMM = 4
+} sq_op;
+
+/*
+ * Step 1 - calibration statistics.
+ * Source: pith.science review of arXiv 2506.01967 (Smooth Rotation),
+ * key_machinery (s_j built from max|X_j| and max|W_j|); SmoothQuant glossary
+ * (dataterminology.com), "What calibration data does SmoothQuant need?"
+ * (statistics from a small calibration set).
+ *
+ *   a      device, [rows x cols] row-major, element type dt, leading dim ld
+ *   axis   0: amax[c] = max_r |a[r,c]|  (X [tokens x Cin] -> amax[Cin])
+ *          1: amax[r] = max_c |a[r,c]|  (W [Cin x Cout] -> amax[Cin])
+ *   accumulate  0: overwrite amax; 1: amax = max(amax, new) (running max
+ *          over calibration batches, or over several weights that share one
+ *          activation, e.g. Q/K/V)
+ *   amax   device fp32, cols (axis 0) or rows (axis 1) entries
+ * NaN inputs propagate: a NaN anywhere makes that channel's statistic NaN
+ * (step 2 then flags it).  rows, cols >= 1.
+ */
+sq_status sq_calibrate_absmax(const void* a, sq_dtype dt, int64_t rows, int64_t cols,
+                              int64_t ld, int axis, int accumulate, float* amax,
+                              cudaStream_t stream);
+
+/*
+ * Step 2 - smoothing factors and their inverses.
+ * Source: Smooth Rotation review, key_machinery (a = 0.5 case,
+ * s_j = sqrt(max|X_j| / max|W_j|)); first page, paragraph 1 (factors finite
+ * and nonzero).  For strength alpha in [0, 1]:
+ *   ax = max(amax_x[j], 1e-5f), aw = max(amax_w[j], 1e-5f)
+ *   s[j] = clamp(RN(ax^alpha) / RN(aw^(1-alpha)), 1e-5f, 1e5f)
+ *   s_inv[j] = 1 / s[j]
+ * Each power is the correctly rounded fp32 value, 1-alpha an fp32
+ * subtraction, each quotient one IEEE fp32 division.  A non-finite
+ * statistic gives s = s_inv = 1 and sets SQ_FLAG_NONFINITE.
+ *   amax_x, amax_w  device fp32 [cin];  s, s_inv  device fp32 [cin]
+ *   dev_flags       device int32 or NULL
+ * alpha outside [0, 1] or not finite -> SQ_ERR_INVALID_ARG.
+ */
+sq_status sq_smooth_factors(const float* amax_x, const float* amax_w, int64_t cin,
+                            float alpha, float* s, float* s_inv, int32_t* dev_flags,
+                            cudaStream_t stream);
+
+/*
+ * Step 3 - offline fold of diag(s) into W's rows, then symmetric INT8
+ * quantization per output channel.
+ * Source: first page, paragraph 1 (S multiplies W); learn-kernels.com
+ * "Quantization", paragraph 2 (transform applied offline, both operands
+ * INT8).  For output channel n:
+ *   W'[j,n] = s[j] * W[j,n]               (fp32 multiply)
+ *   w_scale[n] = max_j |W'[j,n]| / 127    (fp32 division; 1 if the max is 0)
+ *   wq[n,j] = clamp(rne(W'[j,n] * (1 / w_scale[n])), -127, 127)
+ *   w      device [cin x cout] row-major, type dt, leading dim ldw
+ *   s      device fp32 [cin]
+ *   wq     device [cout x cin] codes, row n contiguous (K-major), format fmt
+ *   w_scale device fp32 [cout]
+ *   workspace  device, >= sq_workspace_bytes(SQ_OP_FOLD_QUANTIZE, 0, cout, cin, fmt)
+ * A non-finite column maximum sets SQ_FLAG_NONFINITE.
+ */
+sq_status sq_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin, int64_t cout,
+                                  int64_t ldw, const float* s, void* wq, sq_codes fmt,
+                                  float* w_scale, int32_t* dev_flags, void* workspace,
+                                  size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Step 4 - runtime X diag(s)^-1 fused with dynamic per-token INT8
+ * quantization (one read of X, one write of the codes).
+ * Source: first page, paragraph 3 (the explicit runtime scaling step);
+ * learn-kernels.com "Quantization", paragraph 2 (activations to INT8).
+ * For token t:
+ *   X'[t,j] = X[t,j] * s_inv[j]           (fp32 multiply)
+ *   x_scale[t] = max_j |X'[t,j]| / 127    (fp32 division; 1 if the max is 0)
+ *   xq[t,j] = clamp(rne(X'[t,j] * (1 / x_scale[t])), -127, 127)
+ *   x      device [tokens x cin] row-major, type dt, leading dim ldx
+ *   s_inv  device fp32 [cin] (from step 2)
+ *   xq     device [tokens x cin] codes, row-major, format fmt
+ *   x_scale device fp32 [tokens]
+ * A non-finite token maximum sets SQ_FLAG_NONFINITE (its codes are then
+ * unspecified).
+ */
+sq_status sq_quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                       const float* s_inv, void* xq, sq_codes fmt, float* x_scale,
+                       int32_t* dev_flags, cudaStream_t stream);
+
+/*
+ * Step 5 - INT8 x INT8 GEMM with exact integer accumulation and a bf16
+ * dequantizing epilogue.
+ * Source: learn-kernels.com "Quantization", paragraph 2 (the matmul runs on
+ * INT8 weights and activations on low-precision hardware paths).
+ *   acc[t,n] = sum_j xq[t,j] * wq[n,j]    (exact, |acc| < 2^31)
+ *   y[t,n]   = bf16(acc[t,n] * x_scale[t] * w_scale[n])  (fp32 epilogue;
+ *              within 1 bf16 ulp of the exactly rounded value)
+ *   xq     device [m x k] codes, format fmt (row-major, K contiguous)
+ *   wq     device [n x k] codes, format fmt (K contiguous)
+ *   y      device bf16 [m x n] row-major
+ *   acc_out  device int32 [m x n] or NULL: the exact accumulators
+ *   workspace  device, >= sq_workspace_bytes(SQ_OP_GEMM, m, n, k, fmt)
+ * k must be a multiple of 16.  SQ_CODES_BF16 runs on the tcgen05 tensor
+ * cores (fp32 accumulation in TMEM, converted to int32 every <= 1024
+ * products so every partial sum stays an exact integer); SQ_CODES_I8 runs
+ * on the legacy integer mma.sync path, which suits small m (decode).
+ * A pipeline wait that runs out sets SQ_FLAG_TIMEOUT.
+ */
+sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq,
+                       const float* w_scale, sq_codes fmt, int64_t m, int64_t n, int64_t k,
+                       void* y, int32_t* acc_out, int32_t* dev_flags, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes an operation needs for these sizes (0 if none). */
+size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fmt);
+
+/* Static text for a status code. */
+const char* sq_status_string(sq_status status);
+
+/* SQ_OK if `device` is an sm_103 GPU this library can run on, else
+ * SQ_ERR_UNSUPPORTED (or SQ_ERR_CUDA if the query fails). */
+sq_status sq_check_device(int device);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SQ_B300_H */

@@ -1,0 +1,302 @@
+"""GPU parity: every step of the CUDA path against the CPU oracle.
+
+Each step is fed the oracle's own inputs for that step, so a mismatch
+points at one kernel.  Integer work (statistics bits, factors, codes,
+scales, accumulators) must match bit for bit; the bf16 outputs within one
+bf16 ulp.  Small cases span several tiles and ragged tails; the five
+workloads run at full size in the launch configuration the benchmark times,
+with all codes compared and the GEMM output compared on sampled tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sq_oracle as O
+from w8a8_post_quantization_02_b300 import synth
+
+pytestmark = pytest.mark.gpu
+F32 = np.float32
+
+
+@pytest.fixture(scope="module")
+def sq():
+    from tests._lib_util import ensure_built
+    ensure_built()
+    from w8a8_post_quantization_02_b300 import sq as sqmod
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    sqmod.check_device(torch.cuda.current_device())
+    return sqmod
+
+
+# ------------------------------------------------------------------ helpers
+def dev(a: np.ndarray, dtype: str):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def f32bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy().astype(F32).view(np.uint32)
+
+
+def npbits(a) -> np.ndarray:
+    return np.asarray(a, F32).view(np.uint32)
+
+
+def codes_np(t: torch.Tensor) -> np.ndarray:
+    """int8 codes from either code format (bf16 codes must be exact integers)."""
+    if t.dtype == torch.bfloat16:
+        f = t.float().cpu().numpy()
+        assert np.array_equal(f, np.rint(f)) and np.abs(f).max(initial=0) <= 127
+        return f.astype(np.int8)
+    return t.cpu().numpy()
+
+
+def y_bits(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def flags_tensor():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+SMALL = [
+    dict(name="single_linear", **synth.WORKLOADS["single_linear_64x512x512"]),
+    dict(name="ragged_bf16", tokens=37, cin=80, cout=300, dtype="bf16", outlier_frac=0.05),
+    dict(name="ragged_f32", tokens=129, cin=528, cout=33, dtype="f32", outlier_frac=0.02),
+    dict(name="one_token", tokens=1, cin=256, cout=264, dtype="bf16", outlier_frac=0.02),
+    dict(name="tall_narrow", tokens=300, cin=64, cout=17, dtype="bf16", x_std=0.5, alpha=0.85,
+         fixed_channels=2, fixed_factor=60.0, massive_tokens=3, massive_channels=2),
+    dict(name="multi_tile", tokens=200, cin=1040, cout=520, dtype="bf16", outlier_frac=0.01,
+         alpha=0.8, outlier_lo=30.0, outlier_hi=120.0),
+]
+
+
+def make_small(p):
+    p = dict(p)
+    name = p.pop("name")
+    return synth.make_case(name, **p)
+
+
+# ------------------------------------------------------------------ per-step parity
+@pytest.mark.parametrize("p", SMALL, ids=[p["name"] for p in SMALL])
+def test_calibrate_bit_exact(sq, p):
+    c = make_small(p)
+    x, w = dev(c.x, c.dtype), dev(c.w, c.dtype)
+    ax = sq.calibrate_absmax(x, 0)
+    aw = sq.calibrate_absmax(w, 1)
+    assert np.array_equal(f32bits(ax), npbits(O.calibrate_absmax(c.x_f32(), 0)))
+    assert np.array_equal(f32bits(aw), npbits(O.calibrate_absmax(c.w_f32(), 1)))
+    # column and row reductions of the other matrix too (both axes on both)
+    assert np.array_equal(f32bits(sq.calibrate_absmax(w, 0)), npbits(O.calibrate_absmax(c.w_f32(), 0)))
+    assert np.array_equal(f32bits(sq.calibrate_absmax(x, 1)), npbits(O.calibrate_absmax(c.x_f32(), 1)))
+
+
+@pytest.mark.parametrize("p", SMALL, ids=[p["name"] for p in SMALL])
+def test_smooth_factors_bit_exact(sq, p):
+    c = make_small(p)
+    ax, aw = O.calibrate_absmax(c.x_f32(), 0), O.calibrate_absmax(c.w_f32(), 1)
+    s_ref, si_ref, nf = O.smooth_factors(ax, aw, c.alpha)
+    flags = flags_tensor()
+    s, si = sq.smooth_factors(torch.from_numpy(ax).cuda(), torch.from_numpy(aw).cuda(), c.alpha, flags)
+    assert np.array_equal(f32bits(s), npbits(s_ref))
+    assert np.array_equal(f32bits(si), npbits(si_ref))
+    assert int(flags.item()) == 0 and not nf
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+@pytest.mark.parametrize("p", SMALL, ids=[p["name"] for p in SMALL])
+def test_fold_quantize_bit_exact(sq, p, codes):
+    c = make_small(p)
+    s_ref, _, _ = O.smooth_factors(O.calibrate_absmax(c.x_f32(), 0), O.calibrate_absmax(c.w_f32(), 1), c.alpha)
+    wq_ref, ws_ref, _ = O.fold_quantize_weight(c.w_f32(), s_ref)
+    wq, ws = sq.fold_quantize_weight(dev(c.w, c.dtype), torch.from_numpy(s_ref).cuda(), codes)
+    assert np.array_equal(codes_np(wq), wq_ref)
+    assert np.array_equal(f32bits(ws), npbits(ws_ref))
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+@pytest.mark.parametrize("p", SMALL, ids=[p["name"] for p in SMALL])
+def test_quant_act_bit_exact(sq, p, codes):
+    c = make_small(p)
+    _, si_ref, _ = O.smooth_factors(O.calibrate_absmax(c.x_f32(), 0), O.calibrate_absmax(c.w_f32(), 1), c.alpha)
+    xq_ref, xs_ref, _ = O.quant_act(c.x_f32(), si_ref)
+    flags = flags_tensor()
+    xq, xs = sq.quant_act(dev(c.x, c.dtype), torch.from_numpy(si_ref).cuda(), codes, flags)
+    assert np.array_equal(codes_np(xq), xq_ref)
+    assert np.array_equal(f32bits(xs), npbits(xs_ref))
+    assert int(flags.item()) == 0
+
+
+def gemm_codes(sq, xq_ref, xs_ref, wq_ref, ws_ref, codes):
+    if codes == "bf16":
+        xq = torch.from_numpy(xq_ref.astype(F32)).to(torch.bfloat16).cuda()
+        wq = torch.from_numpy(wq_ref.astype(F32)).to(torch.bfloat16).cuda()
+    else:
+        xq, wq = torch.from_numpy(xq_ref).cuda(), torch.from_numpy(wq_ref).cuda()
+    return sq.w8a8_gemm(xq, torch.from_numpy(xs_ref).cuda(), wq, torch.from_numpy(ws_ref).cuda(),
+                        want_acc=True, flags=flags_tensor())
+
+
+def gemm_code_formats():
+    return ["i8", "bf16"]
+
+
+@pytest.mark.parametrize("codes", gemm_code_formats())
+@pytest.mark.parametrize("p", SMALL, ids=[p["name"] for p in SMALL])
+def test_gemm_exact_acc_and_ulp(sq, p, codes):
+    c = make_small(p)
+    r = O.run_path(c.x_f32(), c.w_f32(), c.alpha)
+    y, acc = gemm_codes(sq, r["xq"], r["x_scale"], r["wq"], r["w_scale"], codes)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), r["acc"])
+    d = O.bf16_ulp_distance(y_bits(y), r["y"])
+    assert d.max() <= 1
+
+
+@pytest.mark.parametrize("p", SMALL[:3], ids=[p["name"] for p in SMALL[:3]])
+def test_whole_path_through_binding(sq, p):
+    c = make_small(p)
+    ref = O.run_path(c.x_f32(), c.w_f32(), c.alpha)
+    for codes in gemm_code_formats():
+        got = sq.smoothquant_linear(dev(c.x, c.dtype), dev(c.w, c.dtype), c.alpha, codes, want_acc=True)
+        for key in ("amax_x", "amax_w", "s", "s_inv", "w_scale", "x_scale"):
+            assert np.array_equal(f32bits(got[key]), npbits(ref[key])), key
+        assert np.array_equal(codes_np(got["wq"]), ref["wq"])
+        assert np.array_equal(codes_np(got["xq"]), ref["xq"])
+        assert np.array_equal(got["acc"].cpu().numpy().astype(np.int64), ref["acc"])
+        assert O.bf16_ulp_distance(y_bits(got["y"]), ref["y"]).max() <= 1
+
+
+# ------------------------------------------------------------------ edge cases
+def test_zero_channel_and_zero_token(sq):
+    c = synth.make_case("z", 24, 64, 40, dtype="bf16", outlier_frac=0.05)
+    x, w = c.x.copy(), c.w.copy()
+    x[:, 5] = 0
+    x[7, :] = 0
+    w[:, 3] = 0   # output channel 3 all zero
+    w[9, :] = 0   # input channel 9 all zero in W
+    xf, wf = synth.bf16_bits_to_f32(x), synth.bf16_bits_to_f32(w)
+    ref = O.run_path(xf, wf, 0.5)
+    got = sq.smoothquant_linear(dev(x, "bf16"), dev(w, "bf16"), 0.5, "i8", want_acc=True)
+    for key in ("s", "s_inv", "w_scale", "x_scale"):
+        assert np.array_equal(f32bits(got[key]), npbits(ref[key])), key
+    assert np.array_equal(codes_np(got["xq"]), ref["xq"])
+    assert np.array_equal(codes_np(got["wq"]), ref["wq"])
+    assert f32bits(got["x_scale"])[7] == npbits([1.0])[0]
+    assert (codes_np(got["wq"])[3] == 0).all()
+
+
+def test_rne_ties_and_clamp_on_gpu(sq):
+    row = np.array([127.0, 2.5, 3.5, -2.5, 0.5, 1.5, -0.5, 126.5, -127.0] + [0.0] * 7, F32)
+    x = torch.from_numpy(row[None, :].copy()).cuda()
+    xq, xs = sq.quant_act(x, torch.ones(16, device="cuda"), "i8")
+    assert xs.item() == 1.0
+    assert codes_np(xq)[0, :9].tolist() == [127, 2, 4, -2, 0, 2, 0, 126, -127]
+
+
+def test_nonfinite_flags(sq):
+    x = torch.randn(8, 32, device="cuda").to(torch.bfloat16)
+    x[3, 4] = float("nan")
+    ax = sq.calibrate_absmax(x, 0)
+    assert torch.isnan(ax[4]) and not torch.isnan(ax[:4]).any()
+    flags = flags_tensor()
+    s, si = sq.smooth_factors(ax, torch.ones(32, device="cuda"), 0.5, flags)
+    assert int(flags.item()) & 1 and s[4].item() == 1.0 and si[4].item() == 1.0
+    flags = flags_tensor()
+    x2 = torch.ones(4, 32, device="cuda")
+    x2[2, 7] = float("inf")
+    sq.quant_act(x2, torch.ones(32, device="cuda"), "i8", flags)
+    assert int(flags.item()) & 1
+
+
+def test_calibration_running_max_and_shared_qkv(sq):
+    c1 = synth.make_case("b1", 40, 96, 16, dtype="bf16", outlier_frac=0.05, seed=1)
+    c2 = synth.make_case("b2", 40, 96, 16, dtype="bf16", outlier_frac=0.05, seed=2)
+    out = sq.calibrate_absmax(dev(c1.x, "bf16"), 0)
+    sq.calibrate_absmax(dev(c2.x, "bf16"), 0, out=out, accumulate=True)
+    ref = O.calibrate_absmax(c2.x_f32(), 0, O.calibrate_absmax(c1.x_f32(), 0))
+    assert np.array_equal(f32bits(out), npbits(ref))
+    # one statistic over Q, K and V: running row max over the three weights
+    qkv = synth.make_case("qkv", 8, 64, (48, 16, 16), dtype="bf16", w_std=0.015)
+    w = qkv.w_f32()
+    parts = [w[:, :48], w[:, 48:64], w[:, 64:]]
+    aw = None
+    for part in parts:
+        t = torch.from_numpy(np.ascontiguousarray(part)).cuda()
+        aw = sq.calibrate_absmax(t, 1) if aw is None else sq.calibrate_absmax(t, 1, out=aw, accumulate=True)
+    assert np.array_equal(f32bits(aw), npbits(O.calibrate_absmax(w, 1)))
+
+
+@pytest.mark.parametrize("codes", gemm_code_formats())
+def test_gemm_saturated_widest_k(sq, codes):
+    """All codes at +-127 with K = 11008: |acc| = 127^2 * 11008 exactly."""
+    k = 11008
+    xq = np.full((3, k), 127, np.int8)
+    xq[1] = -127
+    xq[2, ::2] = -127
+    wq = np.full((5, k), 127, np.int8)
+    wq[4, 1::2] = -127
+    xs = np.array([1e-3, 2.5e-4, 1.0], F32)
+    ws = np.array([1e-4, 3e-4, 1.0, 2.0, 1e-2], F32)
+    y, acc = gemm_codes(sq, xq, xs, wq, ws, codes)
+    ref_acc, ref_y = O.w8a8_gemm(xq, xs, wq, ws)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref_acc)
+    assert ref_acc[0, 0] == 127 * 127 * k
+    assert O.bf16_ulp_distance(y_bits(y), ref_y).max() <= 1
+
+
+@pytest.mark.parametrize("codes", gemm_code_formats())
+@pytest.mark.parametrize("m,n,k", [(1, 8, 16), (1, 1, 4096), (17, 9, 48), (130, 257, 1040), (256, 256, 2048)])
+def test_gemm_shapes_random_codes(sq, codes, m, n, k):
+    u = synth.uniform(m + n + k, 5, (m + n) * k)
+    codes_all = np.clip(np.floor(u * 255.0) - 127.0, -127, 127).astype(np.int8)
+    xq, wq = codes_all[: m * k].reshape(m, k), codes_all[m * k:].reshape(n, k)
+    xs = (0.001 + synth.uniform(1, 6, m)).astype(F32)
+    ws = (0.0001 + synth.uniform(1, 7, n) * 0.01).astype(F32)
+    y, acc = gemm_codes(sq, xq, xs, wq, ws, codes)
+    ref_acc, ref_y = O.w8a8_gemm(xq, xs, wq, ws)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref_acc)
+    assert O.bf16_ulp_distance(y_bits(y), ref_y).max() <= 1
+
+
+# ------------------------------------------------------------------ full-size workloads
+FULL = synth.WORKLOAD_ORDER[1:]
+
+
+def sample_rows(case, k=48):
+    rows = set(np.linspace(0, case.tokens - 1, min(k, case.tokens)).astype(int).tolist())
+    # every massive-outlier token is sampled
+    big = np.nonzero(np.abs(case.x_f32()).max(axis=1) >= 500)[0]
+    rows.update(big.tolist())
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_workload_parity(sq, name):
+    from w8a8_post_quantization_02_b300 import pipeline
+    c = synth.workload(name)
+    ref_ax = O.calibrate_absmax(c.x_f32(), 0)
+    ref_aw = O.calibrate_absmax(c.w_f32(), 1)
+    s_ref, si_ref, _ = O.smooth_factors(ref_ax, ref_aw, c.alpha)
+    wq_ref, ws_ref, _ = O.fold_quantize_weight(c.w_f32(), s_ref)
+    xq_ref, xs_ref, _ = O.quant_act(c.x_f32(), si_ref)
+    rows = sample_rows(c)
+    acc_ref, y_ref = O.w8a8_gemm(xq_ref, xs_ref, wq_ref, ws_ref, rows=rows)
+
+    layer = pipeline.Layer.for_case(c)
+    layer.load(dev(c.x, c.dtype), dev(c.w, c.dtype))
+    layer.step(want_acc=True)
+    torch.cuda.synchronize()
+    assert int(layer.flags.item()) == 0
+    assert np.array_equal(f32bits(layer.amax_x), npbits(ref_ax))
+    assert np.array_equal(f32bits(layer.amax_w), npbits(ref_aw))
+    assert np.array_equal(f32bits(layer.s), npbits(s_ref))
+    assert np.array_equal(f32bits(layer.s_inv), npbits(si_ref))
+    assert np.array_equal(codes_np(layer.wq), wq_ref)
+    assert np.array_equal(f32bits(layer.w_scale), npbits(ws_ref))
+    assert np.array_equal(codes_np(layer.xq), xq_ref)
+    assert np.array_equal(f32bits(layer.x_scale), npbits(xs_ref))
+    rows_t = torch.from_numpy(rows).cuda()
+    assert np.array_equal(layer.acc.index_select(0, rows_t).cpu().numpy().astype(np.int64), acc_ref)
+    y = y_bits(layer.y.index_select(0, rows_t))
+    assert O.bf16_ulp_distance(y, y_ref).max() <= 1

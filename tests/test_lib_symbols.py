@@ -1,0 +1,79 @@
+"""The C-ABI library loads without a GPU and exports every declared entry
+point; host-side argument validation answers without touching a device."""
+import ctypes
+import subprocess
+
+import pytest
+
+from tests._lib_util import declared_symbols, ensure_built
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = ensure_built()
+    from w8a8_post_quantization_02_b300 import sq
+    return path, sq.load_library()
+
+
+def test_header_declares_the_five_steps():
+    syms = declared_symbols()
+    for name in ("sq_calibrate_absmax", "sq_smooth_factors", "sq_fold_quantize_weight",
+                 "sq_quant_act", "sq_w8a8_gemm"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    path, handle = lib
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_symbols():
+        assert name in exported, name
+        assert getattr(handle, name) is not None
+
+
+def test_binding_signatures_cover_the_header():
+    from w8a8_post_quantization_02_b300 import sq
+    assert set(sq.SIGNATURES) == set(declared_symbols())
+
+
+def test_status_strings(lib):
+    _, h = lib
+    assert h.sq_status_string(0) == b"ok"
+    assert h.sq_status_string(1) == b"invalid argument"
+    assert h.sq_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    _, h = lib
+    from w8a8_post_quantization_02_b300 import sq
+    assert h.sq_workspace_bytes(sq.SQ_OP_FOLD_QUANTIZE, 0, 11008, 4096, 0) >= 11008 * 4
+    assert h.sq_workspace_bytes(sq.SQ_OP_QUANT_ACT, 2048, 0, 4096, 0) == 0
+
+
+def test_argument_validation_needs_no_device(lib):
+    _, h = lib
+    from w8a8_post_quantization_02_b300 import sq
+    P = ctypes.c_void_p
+    aligned, odd = P(4096), P(4097)
+    # null input
+    assert h.sq_calibrate_absmax(None, sq.SQ_BF16, 4, 8, 8, 0, 0, aligned, None) == sq.SQ_ERR_INVALID_ARG
+    # ld < cols, bad axis, misaligned base
+    assert h.sq_calibrate_absmax(aligned, sq.SQ_BF16, 4, 8, 4, 0, 0, aligned, None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_calibrate_absmax(aligned, sq.SQ_BF16, 4, 8, 8, 2, 0, aligned, None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_calibrate_absmax(odd, sq.SQ_BF16, 4, 8, 8, 0, 0, aligned, None) == sq.SQ_ERR_INVALID_ARG
+    # alpha outside [0, 1] or NaN
+    for alpha in (-0.1, 1.5, float("nan"), float("inf")):
+        assert h.sq_smooth_factors(aligned, aligned, 8, alpha, aligned, aligned, None, None) == sq.SQ_ERR_INVALID_ARG
+    # cin not a multiple of 16; missing workspace
+    assert h.sq_fold_quantize_weight(aligned, sq.SQ_BF16, 24, 8, 8, aligned, aligned, 0, aligned,
+                                     None, aligned, 4096, None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_fold_quantize_weight(aligned, sq.SQ_BF16, 32, 8, 8, aligned, aligned, 0, aligned,
+                                     None, None, 0, None) == sq.SQ_ERR_WORKSPACE
+    # activation quantization: bad code format, too-wide rows
+    assert h.sq_quant_act(aligned, sq.SQ_BF16, 4, 32, 32, aligned, aligned, 7, aligned, None, None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_quant_act(aligned, sq.SQ_F32, 4, 1 << 20, 1 << 20, aligned, aligned, 0, aligned, None, None) == sq.SQ_ERR_UNSUPPORTED
+    # GEMM: k % 16 != 0, zero m, misaligned operand
+    assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 4, 4, 24, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 0, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_w8a8_gemm(odd, aligned, aligned, aligned, 0, 4, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG

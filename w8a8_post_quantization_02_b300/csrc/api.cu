@@ -1,0 +1,124 @@
+// C ABI entry points: argument validation, workspace sizing and dispatch.
+#include "sq_common.cuh"
+
+namespace sq {
+sq_status calibrate_absmax(const void*, sq_dtype, int64_t, int64_t, int64_t, int, int, float*,
+                           cudaStream_t);
+sq_status smooth_factors(const float*, const float*, int64_t, float, float*, float*, int32_t*,
+                         cudaStream_t);
+sq_status fold_quantize_weight(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*,
+                               void*, sq_codes, float*, int32_t*, void*, cudaStream_t);
+sq_status quant_act(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, void*,
+                    sq_codes, float*, int32_t*, cudaStream_t);
+int64_t quant_act_max_cin(sq_dtype);
+sq_status gemm_i8_mma(const int8_t*, const float*, const int8_t*, const float*, int64_t, int64_t,
+                      int64_t, void*, int32_t*, cudaStream_t);
+sq_status gemm_bf16c_tc(const void*, const float*, const void*, const float*, int64_t, int64_t,
+                        int64_t, void*, int32_t*, int32_t*, cudaStream_t);
+
+namespace {
+bool valid_dtype(sq_dtype d) { return d == SQ_F32 || d == SQ_BF16; }
+bool valid_codes(sq_codes c) { return c == SQ_CODES_I8 || c == SQ_CODES_BF16; }
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+}  // namespace
+}  // namespace sq
+
+using namespace sq;
+
+extern "C" {
+
+const char* sq_status_string(sq_status s) {
+  switch (s) {
+    case SQ_OK: return "ok";
+    case SQ_ERR_INVALID_ARG: return "invalid argument";
+    case SQ_ERR_NONFINITE: return "non-finite value";
+    case SQ_ERR_CUDA: return "CUDA error";
+    case SQ_ERR_UNSUPPORTED: return "unsupported request";
+    case SQ_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+sq_status sq_check_device(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
+    return SQ_ERR_CUDA;
+  return (major == 10 && minor == 3) ? SQ_OK : SQ_ERR_UNSUPPORTED;
+}
+
+size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fmt) {
+  (void)m;
+  (void)k;
+  (void)fmt;
+  switch (op) {
+    case SQ_OP_FOLD_QUANTIZE: return n > 0 ? round256((size_t)n * 4) : 0;
+    default: return 0;
+  }
+}
+
+sq_status sq_calibrate_absmax(const void* a, sq_dtype dt, int64_t rows, int64_t cols, int64_t ld,
+                              int axis, int accumulate, float* amax, cudaStream_t stream) {
+  if (!a || !amax || !valid_dtype(dt) || rows < 1 || cols < 1 || ld < cols ||
+      (axis != 0 && axis != 1) || (accumulate != 0 && accumulate != 1))
+    return SQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a) % elem_bytes(dt)) != 0 || (reinterpret_cast<uintptr_t>(amax) & 3))
+    return SQ_ERR_INVALID_ARG;
+  return calibrate_absmax(a, dt, rows, cols, ld, axis, accumulate, amax, stream);
+}
+
+sq_status sq_smooth_factors(const float* amax_x, const float* amax_w, int64_t cin, float alpha,
+                            float* s, float* s_inv, int32_t* dev_flags, cudaStream_t stream) {
+  if (!amax_x || !amax_w || !s || !s_inv || cin < 1) return SQ_ERR_INVALID_ARG;
+  if (!(alpha >= 0.0f && alpha <= 1.0f)) return SQ_ERR_INVALID_ARG;  // also rejects NaN
+  return smooth_factors(amax_x, amax_w, cin, alpha, s, s_inv, dev_flags, stream);
+}
+
+sq_status sq_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin, int64_t cout,
+                                  int64_t ldw, const float* s, void* wq, sq_codes fmt,
+                                  float* w_scale, int32_t* dev_flags, void* workspace,
+                                  size_t ws_bytes, cudaStream_t stream) {
+  if (!w || !s || !wq || !w_scale || !valid_dtype(dt) || !valid_codes(fmt) || cin < 1 ||
+      cout < 1 || ldw < cout || cin % 16 != 0)
+    return SQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w) % elem_bytes(dt)) != 0 || !aligned16(wq) || (reinterpret_cast<uintptr_t>(s) & 3) ||
+      (reinterpret_cast<uintptr_t>(w_scale) & 3))
+    return SQ_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < sq_workspace_bytes(SQ_OP_FOLD_QUANTIZE, 0, cout, cin, fmt) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 3))
+    return SQ_ERR_WORKSPACE;
+  return fold_quantize_weight(w, dt, cin, cout, ldw, s, wq, fmt, w_scale, dev_flags, workspace,
+                              stream);
+}
+
+sq_status sq_quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                       const float* s_inv, void* xq, sq_codes fmt, float* x_scale,
+                       int32_t* dev_flags, cudaStream_t stream) {
+  if (!x || !s_inv || !xq || !x_scale || !valid_dtype(dt) || !valid_codes(fmt) || tokens < 1 ||
+      cin < 1 || ldx < cin || cin % 16 != 0)
+    return SQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || (ldx * elem_bytes(dt)) % 16 != 0 || !aligned16(xq) || !aligned16(s_inv))
+    return SQ_ERR_INVALID_ARG;
+  if (cin > quant_act_max_cin(dt)) return SQ_ERR_UNSUPPORTED;
+  return quant_act(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, dev_flags, stream);
+}
+
+sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
+                       sq_codes fmt, int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out,
+                       int32_t* dev_flags, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  if (!xq || !x_scale || !wq || !w_scale || !y || !valid_codes(fmt) || m < 1 || n < 1 || k < 16 ||
+      k % 16 != 0)
+    return SQ_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(y) & 3) ||
+      (reinterpret_cast<uintptr_t>(acc_out) & 3))
+    return SQ_ERR_INVALID_ARG;
+  if (fmt == SQ_CODES_I8)
+    return gemm_i8_mma(static_cast<const int8_t*>(xq), x_scale, static_cast<const int8_t*>(wq),
+                       w_scale, m, n, k, y, acc_out, stream);
+  return gemm_bf16c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+// Shared device/host helpers of the sm_103a SmoothQuant W8A8 library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "sq.h"
+
+#define SQ_DEVINL __device__ __forceinline__
+
+namespace sq {
+
+constexpr int kThreads = 256;  // block size of the streaming kernels
+
+// ---------------------------------------------------------------- host side
+inline sq_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SQ_OK : SQ_ERR_CUDA;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int elem_bytes(sq_dtype dt) { return dt == SQ_F32 ? 4 : 2; }
+
+inline int code_bytes(sq_codes f) { return f == SQ_CODES_BF16 ? 2 : 1; }
+
+inline int sm_count() {
+  static int n = 0;  // queried once; the device does not change its SM count
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// ---------------------------------------------------------------- device side
+// 16-byte streaming load that bypasses L1 allocation (read-once data).
+SQ_DEVINL uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16-byte load through the read-only path (reused data such as s_inv).
+SQ_DEVINL uint4 ld_ro16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+SQ_DEVINL void st16(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+SQ_DEVINL void st8(void* p, uint2 v) {
+  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+SQ_DEVINL float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+SQ_DEVINL float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// |x| as ordered bits: for non-negative floats (and NaN, which sorts above
+// +inf) unsigned comparison of the bit patterns orders like the values.
+SQ_DEVINL uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
+
+SQ_DEVINL void raise_flag(int32_t* flags, int32_t bit) {
+  if (flags) atomicOr(flags, bit);
+}
+
+SQ_DEVINL bool finite_bits(uint32_t absb) { return absb < 0x7F800000u; }
+
+// Symmetric INT8 scale for a maximum magnitude: d = amax / 127 (IEEE fp32
+// division), 1 when amax == 0, and its reciprocal 1/d (IEEE division).
+SQ_DEVINL void scale_and_inverse(float amax, float& d, float& inv) {
+  d = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+  inv = __fdiv_rn(1.0f, d);
+}
+
+// rne(clamp(v * inv, -127, 127)) returned as the float v' = code + 1.5*2^23,
+// whose low byte is the two's-complement code and whose value minus
+// 1.5*2^23 is the code exactly.  The add rounds to nearest-even on the
+// integer grid because 1.5*2^23 + [-127.5, 127.5] lies in [2^23, 2^24).
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+SQ_DEVINL float code_magic(float v, float inv) {
+  float q = __fmul_rn(v, inv);
+  q = fminf(fmaxf(q, -127.0f), 127.0f);
+  return __fadd_rn(q, kMagic);
+}
+
+SQ_DEVINL uint32_t magic_to_bf16bits(float m) {
+  // exact integer value as fp32, then its upper half is the exact bf16
+  return __float_as_uint(__fsub_rn(m, kMagic)) >> 16;
+}
+
+// Pack the low bytes of four magic floats into one word (code0 in byte 0).
+SQ_DEVINL uint32_t pack4_codes(float m0, float m1, float m2, float m3) {
+  uint32_t lo = __byte_perm(__float_as_uint(m0), __float_as_uint(m1), 0x0040);
+  uint32_t hi = __byte_perm(__float_as_uint(m2), __float_as_uint(m3), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
+}
+
+SQ_DEVINL uint32_t pack2_bf16codes(float m0, float m1) {
+  return magic_to_bf16bits(m0) | (magic_to_bf16bits(m1) << 16);
+}
+
+}  // namespace sq

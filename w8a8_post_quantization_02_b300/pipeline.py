@@ -1,0 +1,135 @@
+"""One SmoothQuant W8A8 linear layer with preallocated device buffers.
+
+``Layer.step()`` runs the five steps of the path in order on the current
+stream through the C ABI (calibrate X and W, smoothing factors, fold +
+quantize W, quantize X, GEMM) without allocating, so it can be timed and
+captured into a CUDA graph.  The benchmark and the full-size parity tests
+use this same object, so they exercise identical launches.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import sq
+
+# Token count from which the bf16-coded tensor-core GEMM is used; below it
+# the step streams int8 weight codes through the integer mma.sync path.
+TENSOR_PATH_MIN_TOKENS = 64
+
+
+def choose_codes(tokens: int) -> str:
+    return "bf16" if tokens >= TENSOR_PATH_MIN_TOKENS else "i8"
+
+
+class Layer:
+    def __init__(self, tokens: int, cin: int, cout: int, dtype: str, alpha: float,
+                 codes: str | None = None, device="cuda"):
+        self.tokens, self.cin, self.cout = tokens, cin, cout
+        self.dtype = dtype
+        self.alpha = float(alpha)
+        self.codes = codes or choose_codes(tokens)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        cdt = torch.bfloat16 if self.codes == "bf16" else torch.int8
+        dv = torch.device(device)
+        self.x = torch.empty(tokens, cin, dtype=tdt, device=dv)
+        self.w = torch.empty(cin, cout, dtype=tdt, device=dv)
+        self.amax_x = torch.empty(cin, dtype=torch.float32, device=dv)
+        self.amax_w = torch.empty(cin, dtype=torch.float32, device=dv)
+        self.s = torch.empty(cin, dtype=torch.float32, device=dv)
+        self.s_inv = torch.empty(cin, dtype=torch.float32, device=dv)
+        self.wq = torch.empty(cout, cin, dtype=cdt, device=dv)
+        self.w_scale = torch.empty(cout, dtype=torch.float32, device=dv)
+        self.xq = torch.empty(tokens, cin, dtype=cdt, device=dv)
+        self.x_scale = torch.empty(tokens, dtype=torch.float32, device=dv)
+        self.y = torch.empty(tokens, cout, dtype=torch.bfloat16, device=dv)
+        self.acc = torch.empty(tokens, cout, dtype=torch.int32, device=dv)
+        self.flags = torch.zeros(1, dtype=torch.int32, device=dv)
+        fmt = sq._codes_fmt(self.codes)
+        self._fmt = fmt
+        ws_fold = sq.workspace_bytes(sq.SQ_OP_FOLD_QUANTIZE, 0, cout, cin, self.codes)
+        ws_gemm = sq.workspace_bytes(sq.SQ_OP_GEMM, tokens, cout, cin, self.codes)
+        self.ws_fold = torch.empty(max(ws_fold, 256), dtype=torch.uint8, device=dv)
+        self.ws_gemm = torch.empty(max(ws_gemm, 256), dtype=torch.uint8, device=dv)
+        self._lib = sq.load_library()
+
+    @classmethod
+    def for_case(cls, case, codes: str | None = None) -> "Layer":
+        return cls(case.tokens, case.cin, case.cout, case.dtype, case.alpha, codes)
+
+    def load(self, x: torch.Tensor, w: torch.Tensor) -> None:
+        self.x.copy_(x)
+        self.w.copy_(w)
+
+    # bytes one step moves through HBM by definition of each step (the
+    # algorithmic traffic used for the roofline figures)
+    def algorithmic_bytes(self) -> dict:
+        eb = 2 if self.dtype == "bf16" else 4
+        cb = 2 if self.codes == "bf16" else 1
+        T, K, N = self.tokens, self.cin, self.cout
+        return {
+            "calibrate_x": T * K * eb + K * 4,
+            "calibrate_w": K * N * eb + K * 4,
+            "smooth": K * 4 * 4,
+            "fold_quantize": K * N * eb + N * K * cb + N * 4,
+            "quant_act": T * K * eb + T * K * cb + T * 4 + K * 4,
+            "gemm": (T + N) * K * cb + T * N * 2 + (T + N) * 4,
+        }
+
+    def gemm_ops(self) -> int:
+        return 2 * self.tokens * self.cin * self.cout
+
+    def stages(self, want_acc: bool = False):
+        """The path as (name, launches, fn(stream)) in execution order; ``launches``
+        counts the library kernels one call enqueues."""
+        L, P = self._lib, ctypes.c_void_p
+        dt = sq._dtype_code(self.x)
+        T, K, N = self.tokens, self.cin, self.cout
+        ck = sq._check
+        ptr = lambda t: P(t.data_ptr())  # noqa: E731
+        flags = ptr(self.flags)
+
+        def calibrate_x(st):
+            ck("sq_calibrate_absmax", L.sq_calibrate_absmax(ptr(self.x), dt, T, K, K, 0, 0, ptr(self.amax_x), st))
+
+        def calibrate_w(st):
+            ck("sq_calibrate_absmax", L.sq_calibrate_absmax(ptr(self.w), dt, K, N, N, 1, 0, ptr(self.amax_w), st))
+
+        def smooth(st):
+            ck("sq_smooth_factors", L.sq_smooth_factors(ptr(self.amax_x), ptr(self.amax_w), K, self.alpha,
+                                                        ptr(self.s), ptr(self.s_inv), flags, st))
+
+        def fold_quantize(st):
+            ck("sq_fold_quantize_weight", L.sq_fold_quantize_weight(
+                ptr(self.w), dt, K, N, N, ptr(self.s), ptr(self.wq), self._fmt, ptr(self.w_scale), flags,
+                ptr(self.ws_fold), self.ws_fold.numel(), st))
+
+        def quant_act(st):
+            ck("sq_quant_act", L.sq_quant_act(ptr(self.x), dt, T, K, K, ptr(self.s_inv), ptr(self.xq),
+                                              self._fmt, ptr(self.x_scale), flags, st))
+
+        def gemm(st):
+            ck("sq_w8a8_gemm", L.sq_w8a8_gemm(
+                ptr(self.xq), ptr(self.x_scale), ptr(self.wq), ptr(self.w_scale), self._fmt, T, N, K,
+                ptr(self.y), ptr(self.acc) if want_acc else None, flags, ptr(self.ws_gemm),
+                self.ws_gemm.numel(), st))
+
+        return [("calibrate_x", 2, calibrate_x), ("calibrate_w", 1, calibrate_w), ("smooth", 1, smooth),
+                ("fold_quantize", 3, fold_quantize), ("quant_act", 1, quant_act),
+                ("gemm", gemm_launches(self.codes), gemm)]
+
+    def step(self, want_acc: bool = False, stream=None) -> None:
+        st = sq._stream(stream)
+        for _, _, fn in self.stages(want_acc):
+            fn(st)
+
+
+def gemm_launches(codes: str) -> int:
+    """Library kernels one sq_w8a8_gemm call enqueues."""
+    return 1
+
+
+def available_codes():
+    """Code formats whose GEMM path this build runs."""
+    return ["i8", "bf16"]

@@ -6,14 +6,13 @@ CUDA path and the CPU oracle may consume what it produces.
 
 Generator
 ---------
-Counter-based SplitMix64 (Steele, Lea & Flood, "Fast splittable
-pseudorandom number generators", OOPSLA 2014): element ``i`` of stream
-``(seed, tensor_id)`` is ``mix64(key + (i + 1) * GAMMA)`` with
-``key = mix64(seed * 2**32 + tensor_id + GAMMA)``.  Uniforms take the top
-53 bits, ``u = (z >> 11 + 0.5) * 2**-53``, in (0, 1).  Normals use the
-Box-Muller cosine branch on the uniform pair ``(u[2i], u[2i+1])``.
-Values are formed in float64 and rounded once to the tensor dtype with
-round-half-to-even (bf16) or numpy's float32 cast (also RNE).
+numpy's PCG64 bit generator seeded with ``SeedSequence([seed, tensor_id])``,
+one independent stream per drawn tensor; normals from its
+``standard_normal`` and uniforms from ``random``.  Values are formed in
+float64 and rounded once to the tensor dtype with round-half-to-even
+(bf16, below) or numpy's float32 cast (also RNE).  Inputs are generated
+once on the host and handed, bit for bit, to both the CUDA path and the
+oracle.
 
 Workloads
 ---------
@@ -29,48 +28,26 @@ import math
 
 import numpy as np
 
-GAMMA = np.uint64(0x9E3779B97F4A7C15)
-_M1 = np.uint64(0xBF58476D1CE4E5B9)
-_M2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 22
+_CHUNK = 1 << 20
 
 # tensor ids (one independent stream per drawn tensor)
 TID_X, TID_W, TID_XCH, TID_XFAC, TID_TOK, TID_SIGN, TID_W2, TID_W3 = range(1, 9)
 
 
-def _mix64(z: np.ndarray) -> np.ndarray:
-    z = (z ^ (z >> np.uint64(30))) * _M1
-    z = (z ^ (z >> np.uint64(27))) * _M2
-    return z ^ (z >> np.uint64(31))
+def _gen(seed: int, tid: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tid])))
 
 
-def _key(seed: int, tid: int) -> np.uint64:
-    with np.errstate(over="ignore"):
-        base = np.array([(seed << 32) + tid], dtype=np.uint64) + GAMMA
-        return _mix64(base)[0]
-
-
-def raw_u64(seed: int, tid: int, start: int, count: int) -> np.ndarray:
-    """Counter-based SplitMix64 outputs for positions [start, start+count)."""
-    key = _key(seed, tid)
-    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        return _mix64(key + idx * GAMMA)
-
-
-def uniform(seed: int, tid: int, count: int, start: int = 0) -> np.ndarray:
-    z = raw_u64(seed, tid, start, count)
-    return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (2.0 ** -53)
+def uniform(seed: int, tid: int, count: int) -> np.ndarray:
+    """``count`` float64 draws of U(0, 1) from stream (seed, tid)."""
+    return _gen(seed, tid).random(count)
 
 
 def normal(seed: int, tid: int, count: int, std: float = 1.0) -> np.ndarray:
-    """``count`` float64 draws of N(0, std^2), generated in chunks."""
-    out = np.empty(count, dtype=np.float64)
-    for s in range(0, count, _CHUNK):
-        n = min(_CHUNK, count - s)
-        u = uniform(seed, tid, 2 * n, start=2 * s)
-        u1, u2 = u[0::2], u[1::2]
-        out[s:s + n] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2) * std
+    """``count`` float64 draws of N(0, std^2) from stream (seed, tid)."""
+    out = _gen(seed, tid).standard_normal(count)
+    if std != 1.0:
+        out *= std
     return out
 
 
@@ -80,17 +57,25 @@ def f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
     Valid for finite values whose magnitude lies in bf16's normal range
     (the generator never draws anything else; asserted).
     """
-    v = np.ascontiguousarray(v, dtype=np.float64)
-    a = np.abs(v)
-    ok = np.isfinite(v) & ((a == 0) | ((a >= 2.0 ** -126) & (a < 3.3e38)))
-    assert ok.all(), "value outside the bf16 normal range"
-    b = v.view(np.uint64).copy()
+    shape = np.shape(v)
+    v = np.ascontiguousarray(v, dtype=np.float64).ravel()
+    out = np.empty(v.shape, dtype=np.uint16)
     drop = np.uint64(45)  # 52 - 7 explicit mantissa bits
-    lsb = (b >> drop) & np.uint64(1)
-    b = b + (np.uint64((1 << 44) - 1) + lsb)
-    b = b & ~np.uint64((1 << 45) - 1)
-    f32 = b.view(np.float64).astype(np.float32)  # exact: <= 8 significant bits
-    return (f32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    half = np.uint64((1 << 44) - 1)
+    keep = ~np.uint64((1 << 45) - 1)
+    for s in range(0, v.size, _CHUNK):
+        a = v[s:s + _CHUNK]
+        m = np.abs(a)
+        assert np.isfinite(m).all() and (m[m > 0].min(initial=1.0) >= 2.0 ** -126) \
+            and m.max(initial=0.0) < 3.3e38, "value outside the bf16 normal range"
+        b = a.view(np.uint64).copy()
+        lsb = (b >> drop) & np.uint64(1)
+        b += half
+        b += lsb
+        b &= keep
+        f32 = b.view(np.float64).astype(np.float32)  # exact: <= 8 significant bits
+        out[s:s + _CHUNK] = (f32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    return out.reshape(shape)
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
