@@ -16,8 +16,8 @@ blocking or reordering.  Sources (page title, then the passage):
   with X [tokens x Cin] and W [Cin x Cout], Y = XW equals (X S^-1)(S W)
   for a positive invertible diagonal S; scaling the other dimension of W
   is a different map; the factors must be finite and nonzero.
-  Paragraph 3: the runtime multiply by S^-1 (the "extra runtime scaling"
-  step) and one compensation shared by every consumer of an activation.
+  Paragraph 3: an explicit runtime step multiplying activations by S^-1,
+  and one compensation shared by every consumer of an activation.
 * pith.science review of arXiv 2506.01967 ("Smooth Rotation"),
   ``key_machinery``: s_j = sqrt(max|X_j| / max|W_j|) from per-channel
   maxima of activations and weights; ``core_discovery``: symmetric
