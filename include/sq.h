@@ -139,6 +139,32 @@ sq_status sq_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin, int64
                                   size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Step 3 without a caller-provided workspace.  The source pages have no
+ * counterpart; this is a deployment convenience.  Some callers cannot hand
+ * the library device scratch memory: code running inside another engine's
+ * execution callback that receives only a stream and its tensors, or a host
+ * that reserved its whole device-memory budget up front, must not call
+ * cudaMalloc (it can fail for lack of memory or stall every stream on the
+ * device).  This entry point computes exactly what sq_fold_quantize_weight
+ * computes, with the same arguments minus the workspace, and allocates
+ * nothing: its scratch (one 32-bit maximum per output channel) is a fixed
+ * array of SQ_NOALLOC_MAX_COUT entries (256 KiB) in the library's device
+ * memory, which every GPU that loads the library holds until exit.
+ *   - cout > SQ_NOALLOC_MAX_COUT -> SQ_ERR_WORKSPACE (nothing enqueued).
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (e.g. on two streams) race and give wrong results.  Each call clears
+ *     the entries it uses before using them.
+ */
+#define SQ_NOALLOC_MAX_COUT 65536
+sq_status sq_fold_quantize_weight_noalloc(const void* w, sq_dtype dt, int64_t cin, int64_t cout,
+                                          int64_t ldw, const float* s, void* wq, sq_codes fmt,
+                                          float* w_scale, int32_t* dev_flags,
+                                          cudaStream_t stream);
+
+/*
  * Step 4 - runtime X diag(s)^-1 fused with dynamic per-token INT8
  * quantization (one read of X, one write of the codes).
  * Source: first page, paragraph 3 (the explicit runtime scaling step);

@@ -27,6 +27,7 @@ SIGNATURES = {
     "sq_calibrate_absmax": (_I32, [_P, _I32, _I64, _I64, _I64, _I32, _I32, _P, _P]),
     "sq_smooth_factors": (_I32, [_P, _P, _I64, _F, _P, _P, _P, _P]),
     "sq_fold_quantize_weight": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "sq_fold_quantize_weight_noalloc": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_w8a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "sq_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64, _I32]),
