@@ -4,8 +4,11 @@
 One step = the whole path over one layer's synthetic inputs: per-channel
 absmax of X and W, smoothing factors, fold + INT8 quantization of W, fused
 X*S^-1 + per-token INT8 quantization, and the INT8 GEMM with its bf16
-epilogue.  Inputs are resident in HBM before the timed region; L2 is
-flushed (a 256 MiB write, outside the per-step events) before every step.
+epilogue.  The step is replayed as two CUDA graphs (steps 1-4, then the
+GEMM, whose duration gives the roofline figure).  Inputs are resident in
+HBM before the timed region; L2 is flushed (a 256 MiB write, outside the
+per-step events) before every step.  Each kernel is also timed alone, L2
+flushed before it, for its HBM fraction.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead, on a bounded sample of the same workload.  Under torchrun each rank
@@ -222,6 +225,13 @@ def to_device(case, torch):
     return conv(case.x), conv(case.w)
 
 
+# DRAM bytes per launch read back from one ncu capture of the same kernel
+# on the same workload (dram__bytes_read.sum + dram__bytes_write.sum), or
+# absent when the kernel changed after the capture; the capture is summarised
+# in profiles/ under the kernel's and workload's name.
+NCU_TRAFFIC_BYTES = {}
+
+
 def run_ours(args, case_name):
     import torch
     from w8a8_post_quantization_02_b300 import pipeline, sq, synth
@@ -236,23 +246,31 @@ def run_ours(args, case_name):
     stream = torch.cuda.current_stream()
     st = sq._stream(stream)
     stages = layer.stages()
-    names = [s[0] for s in stages]
+    names = [n for n, _, _ in stages]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
-    def one_step(evs=None):
+    # one eager step (library set-up), then the step as two CUDA graphs:
+    # steps 1-4 and the GEMM, so the GEMM's own duration is timed live
+    layer.step()
+    torch.cuda.synchronize()
+    g_pre, g_gemm = layer.capture()
+
+    def one_step(ev=None):
         flush.zero_()
-        if evs is not None:
-            evs[0].record(stream)
-        for i, (_, _, fn) in enumerate(stages):
-            fn(st)
-            if evs is not None:
-                evs[i + 1].record(stream)
+        if ev is not None:
+            ev[0].record(stream)
+        g_pre.replay()
+        if ev is not None:
+            ev[1].record(stream)
+        g_gemm.replay()
+        if ev is not None:
+            ev[2].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         one_step()
     torch.cuda.synchronize()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(local)
     sampler.start()
     barrier(world)
@@ -262,52 +280,65 @@ def run_ours(args, case_name):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
-    per_stage = np.zeros(len(stages))
-    step_ms = np.zeros(K)
-    for i in range(K):
-        for j in range(len(stages)):
-            per_stage[j] += evs[i][j].elapsed_time(evs[i][j + 1])
-        step_ms[i] = evs[i][0].elapsed_time(evs[i][-1])
+    step_ms = np.array([e[0].elapsed_time(e[2]) for e in evs])
+    gemm_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
     total_ms = max_over_ranks(float(step_ms.sum()), world)
     ops = layer.gemm_ops()
     value = world * K * ops / (total_ms * 1e-3) / 1e12
-    stage_us = {n: per_stage[j] / K * 1e3 for j, n in enumerate(names)}
+    gemm_tops = ops / (float(gemm_ms.mean()) * 1e-3) / 1e12
+    if int(layer.flags.item()) != 0:
+        raise RuntimeError(f"device flags raised during the timed steps: {int(layer.flags.item())}")
+
+    # each kernel alone, L2 flushed before it: its HBM roofline fraction
     nbytes = layer.algorithmic_bytes()
     hbm = float(peaks["hbm_gbs"])
+    iso = {}
+    reps = 20
+    for name, _, fn in stages:
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in e:
+            flush.zero_()
+            a.record(stream)
+            fn(st)
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = float(np.median([a.elapsed_time(b) for a, b in e])) * 1e3
+        gbs = nbytes[name] / (us * 1e-6) / 1e9
+        iso[name] = {"us": round(us, 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
+    iso["gemm"]["tops"] = round(ops / (iso["gemm"]["us"] * 1e-6) / 1e12, 2)
+
     bf16_peak = float(peaks["bf16_tflops"])
-    gemm_tops = ops / (stage_us["gemm"] * 1e-6) / 1e12
-    detail = {}
-    for n in names:
-        gbs = nbytes[n] / (stage_us[n] * 1e-6) / 1e9
-        detail[n] = {"us": round(stage_us[n], 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
-    detail["gemm"]["tops"] = round(gemm_tops, 2)
-    launches = sum(s[1] for s in stages) * K
-    tensor_path = layer.codes == "bf16"
-    if tensor_path:
+    if layer.codes == "bf16":
+        kern = "k_gemm_bf16c"
         roofline = {"bound": "tensor", "achieved": gemm_tops, "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": gemm_tops / bf16_peak, "traffic": None, "kernel": "sq_w8a8_gemm (tcgen05, bf16-coded int8)",
-                    "peak_source": f"bf16 dense, {peaks_kind}"}
+                    "frac": gemm_tops / bf16_peak,
+                    "traffic": NCU_TRAFFIC_BYTES.get((kern, case.name)),
+                    "kernel": f"{kern} (sq_w8a8_gemm, tcgen05 kind::f16 on bf16-coded int8)",
+                    "peak_source": f"bf16 dense burst, {peaks_kind}"}
     else:
-        gbs = nbytes["gemm"] / (stage_us["gemm"] * 1e-6) / 1e9
+        kern = "k_gemm_i8_mma"
+        gbs = nbytes["gemm"] / (float(gemm_ms.mean()) * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                    "traffic": None, "kernel": "sq_w8a8_gemm (mma.sync s8)",
+                    "traffic": NCU_TRAFFIC_BYTES.get((kern, case.name)),
+                    "kernel": f"{kern} (sq_w8a8_gemm, mma.sync s8)",
                     "peak_source": f"HBM copy, {peaks_kind}"}
+    launches = layer.kernel_count() * K
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "s8", "data": "synthetic",
         "config": workload_config(case, layer.codes),
         "gemm_tops": gemm_tops,
-        "act_quant_gbs": detail["quant_act"]["gbs"],
-        "act_quant_hbm_frac": detail["quant_act"]["hbm_frac"],
-        "stages": detail,
+        "act_quant_gbs": iso["quant_act"]["gbs"],
+        "act_quant_hbm_frac": iso["quant_act"]["hbm_frac"],
+        "stages_isolated": iso,
         "roofline": roofline,
         "gpu_launches": launches,
         "clocks": clocks,
         "parallelism": f"replicas x{world}",
     }
     if not args.no_e2e:
-        line["e2e"] = run_e2e(layer, stages, x_host, w_host, args.e2e_steps, ops, world, torch)
+        line["e2e"] = run_e2e(layer, g_pre, g_gemm, x_host, w_host, args.e2e_steps, ops, world, torch)
     if rank == 0 and not args.no_cpu_baseline:
         times, o_ops = time_oracle(case, 20.0, min(case.tokens, 256), 3)
         line["cpu_baseline"] = {"value": o_ops * len(times) / sum(times) / 1e12, "unit": "TOPS",
@@ -319,20 +350,18 @@ def run_ours(args, case_name):
     return 0
 
 
-def run_e2e(layer, stages, x_host, w_host, steps, ops, world, torch):
+def run_e2e(layer, g_pre, g_gemm, x_host, w_host, steps, ops, world, torch):
     """Same metric through the public API with host buffers: pinned-host
     H2D of X and W, the whole path, and D2H of Y, every step."""
-    from w8a8_post_quantization_02_b300 import sq
     xh, wh = x_host.pin_memory(), w_host.pin_memory()
     yh = torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()
     stream = torch.cuda.current_stream()
-    st = sq._stream(stream)
 
     def step():
         layer.x.copy_(xh, non_blocking=True)
         layer.w.copy_(wh, non_blocking=True)
-        for _, _, fn in stages:
-            fn(st)
+        g_pre.replay()
+        g_gemm.replay()
         yh.copy_(layer.y, non_blocking=True)
 
     for _ in range(2):

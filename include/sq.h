@@ -92,7 +92,9 @@ typedef enum {
  *          activation, e.g. Q/K/V)
  *   amax   device fp32, cols (axis 0) or rows (axis 1) entries
  * NaN inputs propagate: a NaN anywhere makes that channel's statistic NaN
- * (step 2 then flags it).  rows, cols >= 1.
+ * (step 2 then flags it).  The column reduction's waits for its copies are
+ * bounded; a wait that runs out also leaves NaN statistics behind, so it
+ * too surfaces as SQ_FLAG_NONFINITE in step 2.  rows, cols >= 1.
  */
 sq_status sq_calibrate_absmax(const void* a, sq_dtype dt, int64_t rows, int64_t cols,
                               int64_t ld, int axis, int accumulate, float* amax,
@@ -210,6 +212,19 @@ sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq,
 
 /* Workspace bytes an operation needs for these sizes (0 if none). */
 size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fmt);
+
+/*
+ * Number of kernels one call of `op` enqueues for these sizes, assuming
+ * every pointer is 16-byte aligned: `ld` is the leading dimension (in
+ * elements, type dt) of the call's input matrix, `axis` and `accumulate`
+ * matter for SQ_OP_CALIBRATE only.  Sizes follow each entry point's own
+ * names: calibrate (m = rows, n = cols), smooth (k = cin), fold
+ * (k = cin, n = cout), quant_act (m = tokens, k = cin), GEMM (m, n, k).
+ * For budgeting launches (e.g. in a CUDA graph) and reading a profiler's
+ * launch list.  -1 for an unknown op.
+ */
+int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int64_t ld, int axis,
+                    int accumulate);
 
 /* Static text for a status code. */
 const char* sq_status_string(sq_status status);

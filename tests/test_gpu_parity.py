@@ -259,6 +259,80 @@ def test_gemm_shapes_random_codes(sq, codes, m, n, k):
     assert O.bf16_ulp_distance(y_bits(y), ref_y).max() <= 1
 
 
+
+# ------------------------------------------------------------------ launch-shape coverage
+# Weight shapes that reach every single-pass fold configuration: clusters of
+# 1, 2, 4 and 8 CTAs (Cin up to 1536, 3072, 6144, 12288 rows), a cluster
+# whose last CTA owns no rows (Cin = 6160 with 8 x 896-row CTAs), strips cut
+# short by Cout, fp32 weights, and Cin beyond the single-pass limit (the
+# two-pass path).
+FOLD_SHAPES = [
+    (1536, 96, "bf16"), (1552, 40, "bf16"), (4096, 264, "bf16"), (6160, 72, "bf16"),
+    (12288, 32, "bf16"), (12304, 24, "bf16"), (2048, 20, "f32"), (48, 1000, "f32"),
+]
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+@pytest.mark.parametrize("cin,cout,dtype", FOLD_SHAPES)
+def test_fold_launch_shapes(sq, cin, cout, dtype, codes):
+    c = synth.make_case("fold", 1, cin, cout, dtype=dtype, w_std=0.02, seed=cin + cout)
+    s = (0.25 + 4.0 * synth.uniform(cin, 41, cin)).astype(F32)
+    w = c.w.copy()
+    w[:, cout // 2] = 0   # one all-zero output channel: that strip takes the clamped path
+    wf = synth.bf16_bits_to_f32(w) if dtype == "bf16" else w
+    wq_ref, ws_ref, _ = O.fold_quantize_weight(wf, s)
+    flags = flags_tensor()
+    wq, ws = sq.fold_quantize_weight(dev(w, dtype), torch.from_numpy(s).cuda(), codes, flags)
+    assert int(flags.item()) == 0
+    assert np.array_equal(f32bits(ws), npbits(ws_ref))
+    assert np.array_equal(codes_np(wq), wq_ref)
+
+
+# Activation shapes that reach every block size (128-1024 threads), 1-4
+# vectors per thread, s^-1 in registers and re-read through L1, the largest
+# row (64 KiB), and many rows per CTA (the shared-memory ring wraps).
+ACT_SHAPES = [
+    (1000, 16, "bf16"), (700, 4112, "bf16"), (300, 11008, "bf16"), (40, 32768, "bf16"),
+    (3000, 512, "f32"), (9, 16384, "f32"), (4099, 64, "bf16"),
+]
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+@pytest.mark.parametrize("tokens,cin,dtype", ACT_SHAPES)
+def test_quant_act_launch_shapes(sq, tokens, cin, dtype, codes):
+    c = synth.make_case("act", tokens, cin, 16, dtype=dtype, outlier_frac=0.01, seed=tokens + cin)
+    x = c.x.copy()
+    x[tokens // 3, :] = 0   # an all-zero token takes the clamped path
+    xf = synth.bf16_bits_to_f32(x) if dtype == "bf16" else x
+    si = (0.25 + 4.0 * synth.uniform(cin, 42, cin)).astype(F32)
+    xq_ref, xs_ref, _ = O.quant_act(xf, si)
+    flags = flags_tensor()
+    xq, xs = sq.quant_act(dev(x, dtype), torch.from_numpy(si).cuda(), codes, flags)
+    assert int(flags.item()) == 0
+    assert np.array_equal(f32bits(xs), npbits(xs_ref))
+    assert np.array_equal(codes_np(xq), xq_ref)
+
+
+# Column-maxima shapes for the strip kernel: clusters of 1-8 CTAs, a last
+# CTA with a partial box, a strip cut short by the column count, running
+# maxima over two batches, and a row stride that is not 16-byte aligned
+# (the atomic path).
+COLMAX_SHAPES = [
+    (16, 4096, "bf16"), (2048, 4096, "bf16"), (300, 64, "bf16"), (1000, 40, "f32"),
+    (129, 528, "f32"), (5000, 96, "bf16"), (77, 300, "bf16"),
+]
+
+
+@pytest.mark.parametrize("rows,cols,dtype", COLMAX_SHAPES)
+def test_colmax_launch_shapes(sq, rows, cols, dtype):
+    c1 = synth.make_case("cm1", rows, cols, 8, dtype=dtype, outlier_frac=0.05, seed=rows)
+    c2 = synth.make_case("cm2", rows, cols, 8, dtype=dtype, outlier_frac=0.05, seed=rows + 1)
+    out = sq.calibrate_absmax(dev(c1.x, dtype), 0)
+    assert np.array_equal(f32bits(out), npbits(O.calibrate_absmax(c1.x_f32(), 0)))
+    sq.calibrate_absmax(dev(c2.x, dtype), 0, out=out, accumulate=True)
+    ref = O.calibrate_absmax(c2.x_f32(), 0, O.calibrate_absmax(c1.x_f32(), 0))
+    assert np.array_equal(f32bits(out), npbits(ref))
+
 # ------------------------------------------------------------------ full-size workloads
 FULL = synth.WORKLOAD_ORDER[1:]
 

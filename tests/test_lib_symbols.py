@@ -77,3 +77,17 @@ def test_argument_validation_needs_no_device(lib):
     assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 4, 4, 24, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
     assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 0, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
     assert h.sq_w8a8_gemm(odd, aligned, aligned, aligned, 0, 4, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
+
+
+def test_kernel_counts_need_no_device(lib):
+    _, h = lib
+    from w8a8_post_quantization_02_b300 import sq
+    # fold: one kernel when rows are 16-byte aligned and Cin fits 8 CTAs of
+    # 1536 rows; else the two-pass path (fill, column maxima, quantize)
+    assert h.sq_kernel_count(sq.SQ_OP_FOLD_QUANTIZE, sq.SQ_BF16, 0, 11008, 4096, 11008, 0, 0) == 1
+    assert h.sq_kernel_count(sq.SQ_OP_FOLD_QUANTIZE, sq.SQ_BF16, 0, 4096, 11008, 4096, 0, 0) == 1
+    assert h.sq_kernel_count(sq.SQ_OP_FOLD_QUANTIZE, sq.SQ_BF16, 0, 300, 80, 300, 0, 0) == 3
+    assert h.sq_kernel_count(sq.SQ_OP_FOLD_QUANTIZE, sq.SQ_BF16, 0, 64, 12304, 64, 0, 0) == 3
+    for op in (sq.SQ_OP_SMOOTH, sq.SQ_OP_QUANT_ACT, sq.SQ_OP_GEMM):
+        assert h.sq_kernel_count(op, sq.SQ_BF16, 2048, 11008, 4096, 4096, 0, 0) == 1
+    assert h.sq_kernel_count(99, sq.SQ_BF16, 1, 1, 16, 16, 0, 0) == -1

@@ -7,8 +7,10 @@ sq_fold_quantize_weight_noalloc, whose scratch is a fixed array inside the
 library.  Through the C ABI, two calls in a row must give exactly what the
 workspace-taking sq_fold_quantize_weight gives; the second call uses
 smaller weights than the first, so stale scratch contents from the first
-call would show up as wrong scales.  Collected last so that a stop at the
-first failure has already run every other test.
+call would show up as wrong scales.  Both weights have rows whose length in
+bytes is not a multiple of 16, which sends them down the two-pass fold, the
+path that keeps its per-channel maxima in the scratch array.  Collected
+last so that a stop at the first failure has already run every other test.
 """
 import ctypes
 
@@ -61,7 +63,7 @@ def _no_alloc(sq, w, s, codes):
 @pytest.mark.parametrize("codes", ["i8", "bf16"])
 def test_two_calls_match_the_workspace_entry_point(lib, codes):
     sq = lib
-    big_w, big_s = _weights(1, 512, 1000, 50.0)
+    big_w, big_s = _weights(1, 512, 1004, 50.0)
     small_w, small_s = _weights(2, 256, 700, 1.0)
     for w, s in ((big_w, big_s), (small_w, small_s)):
         wq_ref, ws_ref = _with_workspace(sq, w, s, codes)

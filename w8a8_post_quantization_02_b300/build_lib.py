@@ -7,6 +7,7 @@ binary32 step by step are also compiled with ``-fmad=false``.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import os
 import shutil
 import subprocess
@@ -53,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
-    objs = []
+    objs, cmds = [], []
     for src in SOURCES:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
         cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + COMMON + list(extra_flags)
@@ -61,8 +62,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             cmd.append("-fmad=false")
         if verbose:
             print(" ".join(cmd), flush=True)
-        subprocess.run(cmd, check=True)
+        cmds.append(cmd)
         objs.append(obj)
+    # the translation units are independent: compile them in parallel
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(cmds), os.cpu_count() or 1))) as ex:
+        for r in ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), cmds):
+            if r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise subprocess.CalledProcessError(r.returncode, r.args)
+            if verbose and (r.stdout or r.stderr):
+                sys.stdout.write(r.stdout + r.stderr)
     tmp = LIB + ".tmp"
     cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
     if verbose:

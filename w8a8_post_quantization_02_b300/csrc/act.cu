@@ -6,30 +6,27 @@
 // multiplies activations by S^-1; learn-kernels.com "Quantization",
 // paragraph 2: activations are quantized to INT8.
 //
-// A group of 32-256 threads owns one token row at a time.  The row is read
-// once from HBM with 16-byte streaming loads and kept in registers (up to
-// 16 vectors per thread), scaled by s_inv (L1-resident), reduced to the
-// row's max|X'| (integer max on |x| bits, so NaN/Inf are caught), and
-// quantized from the registers.  HBM traffic per element: one read of X plus one write of the
-// code, and 4 bytes per token for the scale.
-#include "sq_common.cuh"
+// Persistent kernel: each CTA owns every gridDim.x-th token row.  Rows
+// stream from HBM into a ring of shared-memory stages with one-dimensional
+// bulk copies (TMA), several rows ahead of the threads, so the reads of
+// later rows overlap the arithmetic and the code stores of earlier ones.
+// Every thread owns the same column vectors of every row and keeps their
+// s^-1 in registers.  Pass 1 forms X' = X * s^-1 (kept in registers) and
+// the row's max|X'|; one block barrier combines the warps' maxima (and
+// frees the stage for the next copy); pass 2 writes the codes.  HBM
+// traffic per element: one read of X and one write of the code, plus 4
+// bytes per token for the scale.
+#include "sq_async.cuh"
 
 namespace sq {
 namespace {
+using namespace async;
+
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on every mbarrier wait (1 s)
+constexpr int kMaxStages = 8;
 
 template <bool BF16>
-struct ActVec;
-template <>
-struct ActVec<true> {
-  static constexpr int kElems = 8;
-};
-template <>
-struct ActVec<false> {
-  static constexpr int kElems = 4;
-};
-
-template <bool BF16>
-SQ_DEVINL void unpack(uint4 v, float (&f)[ActVec<BF16>::kElems]) {
+SQ_DEVINL void unpack(uint4 v, float* f) {
   if constexpr (BF16) {
     f[0] = bf16lo_to_f32(v.x);
     f[1] = bf16hi_to_f32(v.x);
@@ -47,177 +44,261 @@ SQ_DEVINL void unpack(uint4 v, float (&f)[ActVec<BF16>::kElems]) {
   }
 }
 
-// Max of a u32 over the TPR threads of the block (all get the result).
-template <int TPR>
-SQ_DEVINL uint32_t row_max_u32(uint32_t v, uint32_t* red) {
-  v = __reduce_max_sync(0xFFFFFFFFu, v);
-  if constexpr (TPR == 32) {
-    return v;
-  } else {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    uint32_t r = red[lane < (TPR / 32) ? lane : 0];
-    r = __reduce_max_sync(0xFFFFFFFFu, r);
-    __syncthreads();  // red is reused by the next row
-    return r;
-  }
-}
-
-template <bool BF16>
-SQ_DEVINL void scale_vec(uint4 raw, const float* si_ptr, float (&f)[ActVec<BF16>::kElems]) {
-  constexpr int E = ActVec<BF16>::kElems;
-  unpack<BF16>(raw, f);
+// E consecutive s^-1 values starting at element e0 (16-byte aligned).
+template <int E>
+SQ_DEVINL void load_sinv(const float* s_inv, int64_t e0, float* f) {
 #pragma unroll
   for (int q = 0; q < E; q += 4) {
-    const uint4 si = ld_ro16(si_ptr + q);
-    f[q + 0] = __fmul_rn(f[q + 0], __uint_as_float(si.x));
-    f[q + 1] = __fmul_rn(f[q + 1], __uint_as_float(si.y));
-    f[q + 2] = __fmul_rn(f[q + 2], __uint_as_float(si.z));
-    f[q + 3] = __fmul_rn(f[q + 3], __uint_as_float(si.w));
+    const uint4 v = ld_ro16(s_inv + e0 + q);
+    f[q + 0] = __uint_as_float(v.x);
+    f[q + 1] = __uint_as_float(v.y);
+    f[q + 2] = __uint_as_float(v.z);
+    f[q + 3] = __uint_as_float(v.w);
   }
 }
 
-// A block of TPR threads owns one token row at a time (grid-stride over
-// rows).  Each thread keeps VPT raw 16-byte vectors of X in registers:
-// pass 1 forms X' = X * s_inv and the row's max|X'|, pass 2 recomputes X'
-// from the registers and writes the codes, so X is read from HBM once.
-template <bool BF16, int VPT, int CODES, int TPR>
-__global__ void __launch_bounds__(TPR) k_quant_act(const uint8_t* __restrict__ x, int64_t tokens,
-                                                   int64_t cin, int64_t ldx_bytes,
-                                                   const float* __restrict__ s_inv,
-                                                   uint8_t* __restrict__ xq,
-                                                   float* __restrict__ x_scale, int32_t* flags) {
-  constexpr int E = ActVec<BF16>::kElems;
-  constexpr int CB = CODES == SQ_CODES_BF16 ? 2 : 1;  // bytes per code
-  __shared__ uint32_t red[TPR / 32];
-  const int64_t nvec = cin / E;
-  for (int64_t t = blockIdx.x; t < tokens; t += gridDim.x) {
-    const uint8_t* row = x + t * ldx_bytes;
-    uint4 raw[VPT];
+// NT threads per CTA, each owning VPT 16-byte vectors of every row (vector
+// v = tid + i*NT).  With NT <= 512 the thread's s^-1 values stay in
+// registers; with 1024 threads (rows longer than 32 KiB) the register
+// budget is 64 per thread, so they are re-read through L1 for each row.
+template <bool BF16, int CODES, int NT, int VPT>
+__global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x, int64_t tokens,
+                                                  int nvec, int64_t ldx_bytes,
+                                                  const float* __restrict__ s_inv,
+                                                  uint8_t* __restrict__ xq,
+                                                  float* __restrict__ x_scale, int32_t* flags,
+                                                  int stages) {
+  constexpr int E = BF16 ? 8 : 4;
+  constexpr int NW = NT / 32;
+  constexpr int CB = CODES == SQ_CODES_BF16 ? 2 : 1;
+  constexpr bool kSiReg = NT <= 512;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t row_bytes = (uint32_t)nvec * 16u;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * row_bytes);
+  uint32_t* red = reinterpret_cast<uint32_t*>(full + kMaxStages);  // [2][NW]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  float si[kSiReg ? VPT : 1][E];
+  if constexpr (kSiReg) {
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int64_t v = threadIdx.x + (int64_t)i * TPR;
-      raw[i] = v < nvec ? ld_stream16(row + v * 16) : make_uint4(0u, 0u, 0u, 0u);
+      const int v = tid + i * NT;
+      if (v < nvec) {
+        load_sinv<E>(s_inv, (int64_t)v * E, si[i]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) si[i][e] = 0.0f;
+      }
+    }
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t pol = policy_evict_first();  // X is read once here
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      const int64_t r = blockIdx.x + (int64_t)i * gridDim.x;
+      if (r >= tokens) break;
+      mbar_expect_tx(&full[i], row_bytes);
+      bulk_g2s_hint(smem + (size_t)i * row_bytes, x + r * ldx_bytes, row_bytes, &full[i], pol);
+    }
+  }
+
+  int it = 0;
+  bool aborted = false;
+  for (int64_t r = blockIdx.x; r < tokens; r += gridDim.x, ++it) {
+    const int stage = it % stages;
+    const uint32_t parity = (uint32_t)(it / stages) & 1u;
+    const bool ok = mbar_wait_bounded(&full[stage], parity, kWaitNs);
+    const uint8_t* buf = smem + (size_t)stage * row_bytes;
+
+    // pass 1: X' = X * s^-1 into registers, and the thread's max|X'|
+    float p[VPT][E];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = tid + i * NT;
+      if (ok && v < nvec) {
+        unpack<BF16>(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), p[i]);
+        float sv[E];
+        if constexpr (kSiReg) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) sv[e] = si[i][e];
+        } else {
+          load_sinv<E>(s_inv, (int64_t)v * E, sv);
+        }
+#pragma unroll
+        for (int e = 0; e < E; e += 2) mul2_rn(p[i][e], p[i][e + 1], sv[e], sv[e + 1]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) m = absmax_nan(m, p[i][e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) p[i][e] = 0.0f;
+      }
+    }
+    uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
+    if (lane == 0) red[(it & 1) * NW + warp] = mb;
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    // every thread has read this stage: refill it with the row `stages`
+    // iterations ahead
+    if (tid == 0) {
+      const int64_t rn = r + (int64_t)stages * gridDim.x;
+      if (rn < tokens) {
+        mbar_expect_tx(&full[stage], row_bytes);
+        bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
+      }
     }
     uint32_t amax = 0u;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int64_t v = threadIdx.x + (int64_t)i * TPR;
-      if (v < nvec) {
-        float f[E];
-        scale_vec<BF16>(raw[i], s_inv + v * E, f);
-#pragma unroll
-        for (int e = 0; e < E; ++e) amax = max(amax, abs_bits(f[e]));
-      }
-    }
-    amax = row_max_u32<TPR>(amax, red);
+    for (int w = 0; w < NW; ++w) amax = max(amax, red[(it & 1) * NW + w]);
     float d, inv;
     scale_and_inverse(__uint_as_float(amax), d, inv);
-    if (threadIdx.x == 0) {
-      x_scale[t] = d;
+    if (tid == 0) {
+      x_scale[r] = d;
       if (!finite_bits(amax)) raise_flag(flags, SQ_FLAG_NONFINITE);
     }
-    uint8_t* qrow = xq + t * cin * CB;
+    // With a finite max >= 2^-119, d = RN(amax/127) and 1/d are normal, so
+    // |X' * (1/d)| <= 127 * (1 + 3 * 2^-24) < 127.5 and the clamp to
+    // [-127, 127] can never change a code: it is skipped.
+    const bool no_clamp = amax >= 0x04000000u && amax < 0x7F800000u;
+
+    // pass 2: codes = rne(X' * (1/d)), via the magic-number add
+    uint8_t* qrow = xq + r * (int64_t)nvec * E * CB;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int64_t v = threadIdx.x + (int64_t)i * TPR;
+      const int v = tid + i * NT;
       if (v >= nvec) continue;
-      float f[E], m[E];
-      scale_vec<BF16>(raw[i], s_inv + v * E, f);
+      float q[E];
+      if (no_clamp) {
+        // scalar multiply and add, each with its own rounding: ptxas does
+        // not contract mul.rn/add.rn into a fused multiply-add, which would
+        // round ties of X'/d differently from rne(RN(X' * (1/d)))
 #pragma unroll
-      for (int e = 0; e < E; ++e) m[e] = code_magic(f[e], inv);
-      if constexpr (CODES == SQ_CODES_BF16) {
-        if constexpr (E == 8) {
-          st16(qrow + v * 16, make_uint4(pack2_bf16codes(m[0], m[1]), pack2_bf16codes(m[2], m[3]),
-                                         pack2_bf16codes(m[4], m[5]), pack2_bf16codes(m[6], m[7])));
-        } else {
-          st8(qrow + v * 8, make_uint2(pack2_bf16codes(m[0], m[1]), pack2_bf16codes(m[2], m[3])));
-        }
+        for (int e = 0; e < E; ++e) q[e] = __fadd_rn(__fmul_rn(p[i][e], inv), kMagic);
       } else {
-        if constexpr (E == 8) {
-          st8(qrow + v * 8, make_uint2(pack4_codes(m[0], m[1], m[2], m[3]),
-                                       pack4_codes(m[4], m[5], m[6], m[7])));
-        } else {
-          *reinterpret_cast<uint32_t*>(qrow + v * 4) = pack4_codes(m[0], m[1], m[2], m[3]);
-        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) q[e] = code_magic(p[i][e], inv);
       }
+      if constexpr (CODES == SQ_CODES_BF16) {
+        uint32_t w[E / 2];
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          float c0 = q[e], c1 = q[e + 1];
+          add2_rn(c0, c1, -kMagic, -kMagic);  // exact integers
+          w[e / 2] = __byte_perm(__float_as_uint(c0), __float_as_uint(c1), 0x7632);
+        }
+        if constexpr (E == 8)
+          st16(qrow + (size_t)v * 16, make_uint4(w[0], w[1], w[2], w[3]));
+        else
+          st8(qrow + (size_t)v * 8, make_uint2(w[0], w[1]));
+      } else {
+        if constexpr (E == 8)
+          st8(qrow + (size_t)v * 8,
+              make_uint2(pack4_codes(q[0], q[1], q[2], q[3]), pack4_codes(q[4], q[5], q[6], q[7])));
+        else
+          *reinterpret_cast<uint32_t*>(qrow + (size_t)v * 4) = pack4_codes(q[0], q[1], q[2], q[3]);
+      }
+    }
+  }
+
+  if (aborted && tid == 0) {
+    raise_flag(flags, SQ_FLAG_TIMEOUT);
+    // let every copy this CTA issued land before its shared memory is freed
+    for (int k = 0; k < stages; ++k) {
+      const int j = it + k;
+      if (blockIdx.x + (int64_t)j * gridDim.x >= tokens) break;
+      mbar_wait_bounded(&full[j % stages], (uint32_t)(j / stages) & 1u, 10000000ull);
     }
   }
 }
 
-template <bool BF16, int CODES, int TPR>
-sq_status launch_act_tpr(int vpt, const uint8_t* x, int64_t tokens, int64_t cin, int64_t ldx_bytes,
-                         const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
-                         cudaStream_t st) {
-  // up to 2048 resident threads and 32 resident blocks per SM
-  const int per_sm = std::min(32, 2048 / TPR);
-  const int64_t grid = std::min<int64_t>(tokens, (int64_t)sm_count() * per_sm);
-#define SQ_ACT_CASE(V)                                                                             \
-  case V:                                                                                          \
-    k_quant_act<BF16, V, CODES, TPR><<<(unsigned)grid, TPR, 0, st>>>(x, tokens, cin, ldx_bytes,     \
-                                                                     s_inv, xq, x_scale, flags);   \
-    break;
-  switch (vpt) {
-    SQ_ACT_CASE(1)
-    SQ_ACT_CASE(2)
-    SQ_ACT_CASE(4)
-    SQ_ACT_CASE(8)
-    SQ_ACT_CASE(12)
-    SQ_ACT_CASE(16)
-    default:
-      return SQ_ERR_UNSUPPORTED;
+struct ActLaunch {
+  int stages;
+  size_t smem;
+  int grid;
+};
+
+template <bool BF16, int CODES, int NT, int VPT>
+sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
+                     const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
+                     cudaStream_t st) {
+  auto kern = k_quant_act<BF16, CODES, NT, VPT>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+        cudaSuccess)
+      return SQ_ERR_CUDA;
+    attr_done = true;
   }
-#undef SQ_ACT_CASE
+  const size_t row_bytes = (size_t)nvec * 16;
+  // about 64 KiB of rows in flight per CTA, at least two stages
+  const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, 65536 / row_bytes));
+  const size_t smem = stages * row_bytes + kMaxStages * 8 + 2 * (NT / 32) * 4;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NT, smem) != cudaSuccess)
+    return SQ_ERR_CUDA;
+  occ = std::max(1, std::min(occ, 4));
+  const int64_t grid = std::min<int64_t>(tokens, (int64_t)sm_count() * occ);
+  kern<<<(unsigned)grid, NT, smem, st>>>(x, tokens, nvec, ldx_bytes, s_inv, xq, x_scale, flags,
+                                         stages);
   return launch_status();
 }
 
-int round_vpt(int64_t v) {
-  for (int c : {1, 2, 4, 8, 12, 16})
-    if (v <= c) return c;
-  return 0;
+template <bool BF16, int CODES, int NT>
+sq_status launch_act_nt(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
+                        const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
+                        cudaStream_t st) {
+  switch ((nvec + NT - 1) / NT) {
+    case 1: return launch_act<BF16, CODES, NT, 1>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+    case 2: return launch_act<BF16, CODES, NT, 2>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+    case 3: return launch_act<BF16, CODES, NT, 3>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+    case 4: return launch_act<BF16, CODES, NT, 4>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+    default: return SQ_ERR_UNSUPPORTED;
+  }
 }
 
 template <bool BF16, int CODES>
-sq_status launch_act_codes(int64_t nvec, const uint8_t* x, int64_t tokens, int64_t cin,
-                           int64_t ldx_bytes, const float* s_inv, uint8_t* xq, float* x_scale,
-                           int32_t* flags, cudaStream_t st) {
-  // the narrowest row group (one warp when it fits) whose threads hold the
-  // row in at most 16 vectors each
-  if (nvec <= 32 * 16)
-    return launch_act_tpr<BF16, CODES, 32>(round_vpt((nvec + 31) / 32), x, tokens, cin, ldx_bytes,
-                                           s_inv, xq, x_scale, flags, st);
-  if (nvec <= 64 * 16)
-    return launch_act_tpr<BF16, CODES, 64>(round_vpt((nvec + 63) / 64), x, tokens, cin, ldx_bytes,
-                                           s_inv, xq, x_scale, flags, st);
-  if (nvec <= 128 * 16)
-    return launch_act_tpr<BF16, CODES, 128>(round_vpt((nvec + 127) / 128), x, tokens, cin,
-                                            ldx_bytes, s_inv, xq, x_scale, flags, st);
-  return launch_act_tpr<BF16, CODES, 256>(round_vpt((nvec + 255) / 256), x, tokens, cin, ldx_bytes,
-                                          s_inv, xq, x_scale, flags, st);
+sq_status launch_act_codes(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
+                           const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
+                           cudaStream_t st) {
+  // the smallest block whose threads hold the row in at most 4 vectors each
+  if (nvec <= 128 * 4)
+    return launch_act_nt<BF16, CODES, 128>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+  if (nvec <= 256 * 4)
+    return launch_act_nt<BF16, CODES, 256>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+  if (nvec <= 512 * 4)
+    return launch_act_nt<BF16, CODES, 512>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+  return launch_act_nt<BF16, CODES, 1024>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
 }
 
 }  // namespace
 
-// Largest Cin held in registers: 16 vectors x 256 threads x (8 bf16 | 4 f32).
-int64_t quant_act_max_cin(sq_dtype dt) { return (int64_t)16 * 256 * (dt == SQ_BF16 ? 8 : 4); }
+// Largest Cin: a 64 KiB row (two stages fit one CTA's shared memory), i.e.
+// 4096 vectors of 16 bytes held by 1024 threads x 4.
+int64_t quant_act_max_cin(sq_dtype dt) { return (int64_t)4096 * (dt == SQ_BF16 ? 8 : 4); }
 
 sq_status quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
                     const float* s_inv, void* xq, sq_codes fmt, float* x_scale, int32_t* flags,
                     cudaStream_t st) {
   const bool bf16 = dt == SQ_BF16;
-  const int64_t nvec = cin / (bf16 ? 8 : 4);
+  const int nvec = (int)(cin / (bf16 ? 8 : 4));
   const uint8_t* xb = static_cast<const uint8_t*>(x);
   uint8_t* qb = static_cast<uint8_t*>(xq);
   const int64_t ldb = ldx * elem_bytes(dt);
   if (bf16) {
     return fmt == SQ_CODES_BF16
-               ? launch_act_codes<true, SQ_CODES_BF16>(nvec, xb, tokens, cin, ldb, s_inv, qb, x_scale, flags, st)
-               : launch_act_codes<true, SQ_CODES_I8>(nvec, xb, tokens, cin, ldb, s_inv, qb, x_scale, flags, st);
+               ? launch_act_codes<true, SQ_CODES_BF16>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st)
+               : launch_act_codes<true, SQ_CODES_I8>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st);
   }
   return fmt == SQ_CODES_BF16
-             ? launch_act_codes<false, SQ_CODES_BF16>(nvec, xb, tokens, cin, ldb, s_inv, qb, x_scale, flags, st)
-             : launch_act_codes<false, SQ_CODES_I8>(nvec, xb, tokens, cin, ldb, s_inv, qb, x_scale, flags, st);
+             ? launch_act_codes<false, SQ_CODES_BF16>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st)
+             : launch_act_codes<false, SQ_CODES_I8>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st);
 }
 
 }  // namespace sq

@@ -11,6 +11,8 @@ sq_status fold_quantize_weight(const void*, sq_dtype, int64_t, int64_t, int64_t,
 sq_status quant_act(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, void*,
                     sq_codes, float*, int32_t*, cudaStream_t);
 int64_t quant_act_max_cin(sq_dtype);
+int fold_kernel_count(sq_dtype, int64_t, int64_t, int64_t);
+int calibrate_kernel_count(sq_dtype, int64_t, int64_t, int64_t, int, int);
 sq_status gemm_i8_mma(const int8_t*, const float*, const int8_t*, const float*, int64_t, int64_t,
                       int64_t, void*, int32_t*, cudaStream_t);
 sq_status gemm_bf16c_tc(const void*, const float*, const void*, const float*, int64_t, int64_t,
@@ -55,6 +57,18 @@ size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fm
     case SQ_OP_FOLD_QUANTIZE: return n > 0 ? round256((size_t)n * 4) : 0;
     default: return 0;
   }
+}
+
+int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int64_t ld, int axis,
+                    int accumulate) {
+  switch (op) {
+    case SQ_OP_CALIBRATE: return calibrate_kernel_count(dt, m, n, ld, axis, accumulate);
+    case SQ_OP_SMOOTH: return 1;
+    case SQ_OP_FOLD_QUANTIZE: return fold_kernel_count(dt, k, n, ld);
+    case SQ_OP_QUANT_ACT: return 1;
+    case SQ_OP_GEMM: return 1;
+  }
+  return -1;
 }
 
 sq_status sq_calibrate_absmax(const void* a, sq_dtype dt, int64_t rows, int64_t cols, int64_t ld,

@@ -6,13 +6,24 @@
 // learn-kernels.com "Quantization", paragraph 2: the transform is applied
 // offline and the weights are quantized to INT8.
 //
-// Pass 1 streams W once and reduces max_j |s_j * W[j,n]| per output
-// channel n (8 warps per block over rows, one atomicMax per column per
-// block, into a caller-provided workspace).  Pass 2 streams W again in
-// 64 x 64 tiles, recomputes W' = s_j * W[j,n], quantizes with the channel's
-// 1/d, transposes through shared memory and writes each output channel's
-// codes contiguously.
-#include "sq_common.cuh"
+// Single-pass path (rows of W 16-byte aligned, Cin <= 12288): W is cut into
+// strips of 64 bytes of columns (32 bf16 / 16 fp32 output channels).  A
+// cluster of 1-8 CTAs owns one strip and splits its rows; each CTA loads its
+// part of the strip into shared memory with 2-D TMA copies (64-byte
+// swizzle, so both passes over it are free of bank conflicts), reduces
+// max_j |s_j * W[j,n]| over its rows, and the cluster combines the partial
+// maxima through distributed shared memory.  Each CTA then quantizes its
+// rows from shared memory and writes each output channel's codes as
+// contiguous runs.  W is read from HBM once and the codes written once.
+//
+// Two-pass path (any alignment or width): pass 1 streams W and reduces
+// the column maxima (one atomicMax per column per block, into the caller's
+// workspace); pass 2 streams W again in 64 x 64 tiles, quantizes, transposes
+// through shared memory and writes the codes.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "sq_async.cuh"
 
 namespace sq {
 
@@ -182,11 +193,341 @@ __global__ void __launch_bounds__(kThreads) k_fold_quant(const uint8_t* __restri
   }
 }
 
+
+// ---------------------------------------------------------------- single pass
+namespace strip {
+using namespace async;
+
+constexpr int kThreads = 256;
+constexpr int kBoxRows = 128;                       // rows per TMA box
+constexpr int kRowBytes = 64;                       // strip row = 64 bytes (64-byte swizzle)
+constexpr int kMaxRows = 1536;                      // rows per CTA: 96 KiB of strip
+constexpr int kMaxBoxes = kMaxRows / kBoxRows;
+constexpr uint64_t kWaitNs = 1000000000ull;         // bound on every mbarrier wait (1 s)
+
+// Byte offset of 16-byte chunk c of strip row r in the TMA 64-byte swizzle:
+// the chunk index is XOR-ed with bits 1-2 of the row.
+SQ_DEVINL uint32_t chunk_off(int r, int c) {
+  return (uint32_t)r * kRowBytes + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4);
+}
+
+template <bool BF16>
+SQ_DEVINL void unpack_chunk(uint4 v, float* f) {
+  if constexpr (BF16) {
+    f[0] = bf16lo_to_f32(v.x);
+    f[1] = bf16hi_to_f32(v.x);
+    f[2] = bf16lo_to_f32(v.y);
+    f[3] = bf16hi_to_f32(v.y);
+    f[4] = bf16lo_to_f32(v.z);
+    f[5] = bf16hi_to_f32(v.z);
+    f[6] = bf16lo_to_f32(v.w);
+    f[7] = bf16hi_to_f32(v.w);
+  } else {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+}
+
+template <int EPC>
+struct Layout {
+  static constexpr int SW = 4 * EPC;  // output channels per strip
+  size_t strip, s, red, part, inv, flag, bars, total;
+  explicit __host__ __device__ Layout(int rows_per_cta) {
+    strip = 0;                                     // 1024-aligned base
+    s = strip + (size_t)rows_per_cta * kRowBytes;  // fp32 [R]
+    red = s + (size_t)rows_per_cta * 4;            // u32 [8 warps][4 chunks][EPC]
+    part = red + 8 * 4 * EPC * 4;                  // u32 [SW], read by the whole cluster
+    inv = part + SW * 4;                           // fp32 [SW]
+    flag = inv + SW * 4;                           // int: some channel needs the clamp
+    bars = (flag + 4 + 7) & ~size_t(7);            // mbarriers [kMaxBoxes]
+    total = bars + kMaxBoxes * 8;
+  }
+};
+
+// One CTA of a CL-CTA cluster: rows [rank*R, rank*R + R) of the strip of
+// output channels [n0, n0 + SW).
+template <bool BF16, int CODES, int CL>
+__global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__ CUtensorMap map_w,
+                                                         const float* __restrict__ s, int64_t cin,
+                                                         int64_t cout, int rows_per_cta,
+                                                         uint8_t* __restrict__ wq,
+                                                         float* __restrict__ w_scale,
+                                                         int32_t* flags) {
+  constexpr int EPC = BF16 ? 8 : 4;  // elements per 16-byte chunk
+  constexpr int SW = 4 * EPC;
+  constexpr int CB = CODES == SQ_CODES_BF16 ? 2 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const Layout<EPC> L(rows_per_cta);
+  uint8_t* strip = base + L.strip;
+  float* s_sm = reinterpret_cast<float*>(base + L.s);
+  uint32_t* red = reinterpret_cast<uint32_t*>(base + L.red);
+  uint32_t* part = reinterpret_cast<uint32_t*>(base + L.part);
+  float* inv_sm = reinterpret_cast<float*>(base + L.inv);
+  int* clamp_flag = reinterpret_cast<int*>(base + L.flag);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+  const int64_t n0 = (int64_t)(blockIdx.x / CL) * SW;
+  const int64_t j0 = (int64_t)rank * rows_per_cta;
+  const int64_t left = cin - j0;
+  const int rows = left <= 0 ? 0 : (int)(left < rows_per_cta ? left : rows_per_cta);  // multiple of 16
+  const int nbox = (rows + kBoxRows - 1) / kBoxRows;
+
+  if (tid == 0) {
+    for (int b = 0; b < nbox; ++b) mbar_init(&bars[b], 1);
+    *clamp_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&map_w);
+    for (int b = 0; b < nbox; ++b) {
+      mbar_expect_tx(&bars[b], kBoxRows * kRowBytes);
+      tma_load_2d(strip + (size_t)b * kBoxRows * kRowBytes, &map_w, &bars[b], (int)n0,
+                  (int)(j0 + b * kBoxRows));
+    }
+  }
+  for (int i = tid; i < rows; i += kThreads) s_sm[i] = s[j0 + i];
+  __syncthreads();
+
+  // ---- pass 1: max over this CTA's rows of |s_j * W[j, n]| per channel.
+  // 8 consecutive lanes read 8 consecutive rows of one chunk: conflict-free.
+  bool ok = true;
+  {
+    const int c = (tid >> 3) & 3;
+    const int rsub = (tid & 7) + 8 * warp;  // 0..63
+    float m[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) m[e] = 0.0f;
+    for (int b = 0; b < nbox; ++b) {
+      ok = mbar_wait_bounded(&bars[b], 0, kWaitNs) && ok;
+      const int r1 = min(rows, (b + 1) * kBoxRows);
+      for (int r = b * kBoxRows + rsub; r < r1; r += 64) {
+        float f[EPC];
+        unpack_chunk<BF16>(*reinterpret_cast<const uint4*>(strip + chunk_off(r, c)), f);
+        const float sj = s_sm[r];
+#pragma unroll
+        for (int e = 0; e < EPC; e += 2) mul2_rn(f[e], f[e + 1], sj, sj);
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) m[e] = absmax_nan(m[e], f[e]);
+      }
+    }
+    uint32_t mb[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) {
+      mb[e] = __float_as_uint(m[e]) & 0x7FFFFFFFu;
+      mb[e] = max(mb[e], __shfl_xor_sync(0xFFFFFFFFu, mb[e], 1));
+      mb[e] = max(mb[e], __shfl_xor_sync(0xFFFFFFFFu, mb[e], 2));
+      mb[e] = max(mb[e], __shfl_xor_sync(0xFFFFFFFFu, mb[e], 4));
+    }
+    if ((lane & 7) == 0) {
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) red[(warp * 4 + c) * EPC + e] = mb[e];
+    }
+  }
+  __syncthreads();
+  if (tid < SW) {
+    uint32_t v = 0u;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v = max(v, red[w * SW + tid]);
+    part[tid] = v;
+  }
+  // ---- combine the cluster's partial maxima (distributed shared memory)
+  if constexpr (CL > 1) {
+    cluster_arrive();
+    cluster_wait();
+  } else {
+    __syncthreads();
+  }
+  if (tid < SW) {
+    uint32_t v = 0u;
+    if constexpr (CL > 1) {
+      const uint32_t a = su32(&part[tid]);
+#pragma unroll
+      for (int q = 0; q < CL; ++q) v = max(v, ld_cluster_u32(mapa(a, (uint32_t)q)));
+    } else {
+      v = part[tid];
+    }
+    float d, inv;
+    scale_and_inverse(__uint_as_float(v), d, inv);
+    inv_sm[tid] = inv;
+    const int64_t n = n0 + tid;
+    if (n < cout) {
+      // a finite maximum >= 2^-119 keeps |W' / d| below 127.5, so the clamp
+      // cannot change a code (see the activation kernel)
+      if (!(v >= 0x04000000u && v < 0x7F800000u)) *clamp_flag = 1;
+      if (rank == 0) {
+        w_scale[n] = d;
+        if (!finite_bits(v)) raise_flag(flags, SQ_FLAG_NONFINITE);
+      }
+    }
+  }
+  if constexpr (CL > 1) cluster_arrive();  // done reading the peers' shared memory
+  __syncthreads();
+
+  // ---- pass 2: codes of 8 consecutive rows x one chunk per thread
+  {
+    const int c = tid & 3;
+    const bool clamp = *clamp_flag != 0;
+    float inv[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) inv[e] = inv_sm[c * EPC + e];
+    for (int g = tid >> 2; g * 8 < rows; g += kThreads / 4) {
+      float q[8][EPC];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = g * 8 + k;
+        unpack_chunk<BF16>(*reinterpret_cast<const uint4*>(strip + chunk_off(r, c)), q[k]);
+        const float sj = s_sm[r];
+#pragma unroll
+        for (int e = 0; e < EPC; e += 2) mul2_rn(q[k][e], q[k][e + 1], sj, sj);
+        if (!clamp) {
+          // scalar multiply then add (never contracted into a fused
+          // multiply-add, which would round ties differently)
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) q[k][e] = __fadd_rn(__fmul_rn(q[k][e], inv[e]), kMagic);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) q[k][e] = code_magic(q[k][e], inv[e]);
+        }
+      }
+      const int64_t jrow = j0 + (int64_t)g * 8;
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) {
+        const int64_t n = n0 + c * EPC + e;
+        if (n >= cout) continue;
+        uint8_t* dst = wq + (n * cin + jrow) * CB;
+        if constexpr (CODES == SQ_CODES_BF16) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) {
+            float c0 = q[k][e], c1 = q[k + 1][e];
+            add2_rn(c0, c1, -kMagic, -kMagic);  // exact integers
+            w4[k / 2] = __byte_perm(__float_as_uint(c0), __float_as_uint(c1), 0x7632);
+          }
+          st16(dst, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+        } else {
+          st8(dst, make_uint2(pack4_codes(q[0][e], q[1][e], q[2][e], q[3][e]),
+                              pack4_codes(q[4][e], q[5][e], q[6][e], q[7][e])));
+        }
+      }
+    }
+  }
+
+  if (!ok && tid == 0) {
+    raise_flag(flags, SQ_FLAG_TIMEOUT);
+    for (int b = 0; b < nbox; ++b) mbar_wait_bounded(&bars[b], 0, 10000000ull);
+  }
+  if constexpr (CL > 1) cluster_wait();  // peers may still read `part` until here
+}
+
+// Rows per CTA for cluster size cl (a multiple of the TMA box height).
+int64_t rows_per_cta(int64_t cin, int cl) {
+  const int64_t r = (cin + cl - 1) / cl;
+  return (r + kBoxRows - 1) / kBoxRows * kBoxRows;
+}
+
+template <bool BF16, int CODES, int CL>
+sq_status launch(const CUtensorMap& map, const float* s, int64_t cin, int64_t cout, int rpc,
+                 uint8_t* wq, float* w_scale, int32_t* flags, cudaStream_t st) {
+  constexpr int EPC = BF16 ? 8 : 4;
+  auto kern = k_fold_strip<BF16, CODES, CL>;
+  const size_t smem = Layout<EPC>(rpc).total + 1024;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Layout<EPC>(kMaxRows).total + 1024) != cudaSuccess)
+      return SQ_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t strips = (cout + 4 * EPC - 1) / (4 * EPC);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(strips * CL), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, map, s, cin, cout, rpc, wq, w_scale, flags) != cudaSuccess)
+    return SQ_ERR_CUDA;
+  return launch_status();
+}
+
+template <bool BF16, int CODES>
+sq_status launch_cl(int cl, const CUtensorMap& map, const float* s, int64_t cin, int64_t cout,
+                    int rpc, uint8_t* wq, float* w_scale, int32_t* flags, cudaStream_t st) {
+  switch (cl) {
+    case 1: return launch<BF16, CODES, 1>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+    case 2: return launch<BF16, CODES, 2>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+    case 4: return launch<BF16, CODES, 4>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+    default: return launch<BF16, CODES, 8>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+  }
+}
+
+int cluster_size(int64_t cin) {
+  for (int c : {1, 2, 4, 8})
+    if (rows_per_cta(cin, c) <= kMaxRows) return c;
+  return 0;
+}
+
+bool applies(sq_dtype dt, int64_t cin, int64_t cout, int64_t ldw) {
+  return (ldw * elem_bytes(dt)) % 16 == 0 && cin <= ((int64_t)1 << 30) &&
+         cout <= ((int64_t)1 << 30) && cluster_size(cin) != 0;
+}
+
+// SQ_ERR_UNSUPPORTED when the single-pass path does not apply (the caller
+// then takes the two-pass path); otherwise the launch status.
+sq_status fold_single_pass(const void* w, sq_dtype dt, int64_t cin, int64_t cout, int64_t ldw,
+                           const float* s, void* wq, sq_codes fmt, float* w_scale, int32_t* flags,
+                           cudaStream_t st) {
+  const int eb = elem_bytes(dt);
+  if (!aligned16(w) || !applies(dt, cin, cout, ldw)) return SQ_ERR_UNSUPPORTED;
+  const int cl = cluster_size(cin);
+  const int rpc = (int)rows_per_cta(cin, cl);
+  auto fn = tensor_map_encoder();
+  if (!fn) return SQ_ERR_CUDA;
+  CUtensorMap map;
+  cuuint64_t dims[2] = {(cuuint64_t)cout, (cuuint64_t)cin};
+  cuuint64_t strides[1] = {(cuuint64_t)(ldw * eb)};
+  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / eb), (cuuint32_t)kBoxRows};
+  cuuint32_t estr[2] = {1, 1};
+  if (fn(&map, dt == SQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+         const_cast<void*>(w), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SQ_ERR_CUDA;
+  uint8_t* q = static_cast<uint8_t*>(wq);
+  if (dt == SQ_BF16)
+    return fmt == SQ_CODES_BF16
+               ? launch_cl<true, SQ_CODES_BF16>(cl, map, s, cin, cout, rpc, q, w_scale, flags, st)
+               : launch_cl<true, SQ_CODES_I8>(cl, map, s, cin, cout, rpc, q, w_scale, flags, st);
+  return fmt == SQ_CODES_BF16
+             ? launch_cl<false, SQ_CODES_BF16>(cl, map, s, cin, cout, rpc, q, w_scale, flags, st)
+             : launch_cl<false, SQ_CODES_I8>(cl, map, s, cin, cout, rpc, q, w_scale, flags, st);
+}
+
+}  // namespace strip
+
 }  // namespace
+
+int fold_kernel_count(sq_dtype dt, int64_t cin, int64_t cout, int64_t ldw) {
+  return strip::applies(dt, cin, cout, ldw) ? 1 : 3;
+}
 
 sq_status fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin, int64_t cout, int64_t ldw,
                                const float* s, void* wq, sq_codes fmt, float* w_scale,
                                int32_t* flags, void* workspace, cudaStream_t st) {
+  {
+    const sq_status r = strip::fold_single_pass(w, dt, cin, cout, ldw, s, wq, fmt, w_scale, flags, st);
+    if (r != SQ_ERR_UNSUPPORTED) return r;
+  }
   const bool bf16 = dt == SQ_BF16;
   const uint8_t* wb = static_cast<const uint8_t*>(w);
   const int64_t ldb = ldw * elem_bytes(dt);

@@ -83,6 +83,7 @@ class Layer:
     def stages(self, want_acc: bool = False):
         """The path as (name, launches, fn(stream)) in execution order; ``launches``
         counts the library kernels one call enqueues."""
+        counts = self.kernel_counts()
         L, P = self._lib, ctypes.c_void_p
         dt = sq._dtype_code(self.x)
         T, K, N = self.tokens, self.cin, self.cout
@@ -115,19 +116,49 @@ class Layer:
                 ptr(self.y), ptr(self.acc) if want_acc else None, flags, ptr(self.ws_gemm),
                 self.ws_gemm.numel(), st))
 
-        return [("calibrate_x", 2, calibrate_x), ("calibrate_w", 1, calibrate_w), ("smooth", 1, smooth),
-                ("fold_quantize", 3, fold_quantize), ("quant_act", 1, quant_act),
-                ("gemm", gemm_launches(self.codes), gemm)]
+        fns = [("calibrate_x", calibrate_x), ("calibrate_w", calibrate_w), ("smooth", smooth),
+               ("fold_quantize", fold_quantize), ("quant_act", quant_act), ("gemm", gemm)]
+        return [(name, counts[name], fn) for name, fn in fns]
+
+    def kernel_counts(self) -> dict:
+        """Library kernels each stage of one step enqueues (the library's own count)."""
+        dt = sq.SQ_BF16 if self.dtype == "bf16" else sq.SQ_F32
+        T, K, N = self.tokens, self.cin, self.cout
+        return {
+            "calibrate_x": sq.kernel_count(sq.SQ_OP_CALIBRATE, dt, T, K, 0, K, 0, False),
+            "calibrate_w": sq.kernel_count(sq.SQ_OP_CALIBRATE, dt, K, N, 0, N, 1, False),
+            "smooth": sq.kernel_count(sq.SQ_OP_SMOOTH, dt, 0, 0, K),
+            "fold_quantize": sq.kernel_count(sq.SQ_OP_FOLD_QUANTIZE, dt, 0, N, K, N),
+            "quant_act": sq.kernel_count(sq.SQ_OP_QUANT_ACT, dt, T, 0, K, K),
+            "gemm": sq.kernel_count(sq.SQ_OP_GEMM, dt, T, N, K),
+        }
+
+    def kernel_count(self) -> int:
+        """Library kernels one step enqueues."""
+        return sum(self.kernel_counts().values())
 
     def step(self, want_acc: bool = False, stream=None) -> None:
         st = sq._stream(stream)
         for _, _, fn in self.stages(want_acc):
             fn(st)
 
-
-def gemm_launches(codes: str) -> int:
-    """Library kernels one sq_w8a8_gemm call enqueues."""
-    return 1
+    def capture(self, want_acc: bool = False):
+        """Two CUDA graphs of one step: steps 1-4 (calibration through the
+        activation codes) and the GEMM, replayed with ``graph.replay()`` on
+        the current stream.  Call ``step()`` once first, outside capture, so
+        the library's one-time set-up (kernel attributes) is done."""
+        stages = self.stages(want_acc)
+        pre = [fn for name, _, fn in stages if name != "gemm"]
+        gemm = [fn for name, _, fn in stages if name == "gemm"]
+        graphs = []
+        for fns in (pre, gemm):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                st = sq._stream()
+                for fn in fns:
+                    fn(st)
+            graphs.append(g)
+        return graphs[0], graphs[1]
 
 
 def available_codes():

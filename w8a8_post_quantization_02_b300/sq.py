@@ -31,6 +31,7 @@ SIGNATURES = {
     "sq_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_w8a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "sq_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64, _I32]),
+    "sq_kernel_count": (_I32, [_I32, _I32, _I64, _I64, _I64, _I64, _I32, _I32]),
     "sq_status_string": (ctypes.c_char_p, [_I32]),
     "sq_check_device": (_I32, [_I32]),
 }
@@ -101,6 +102,12 @@ def check_device(device: int = 0) -> None:
 
 def workspace_bytes(op: int, m: int, n: int, k: int, codes: str = "i8") -> int:
     return int(load_library().sq_workspace_bytes(op, m, n, k, _codes_fmt(codes)))
+
+
+def kernel_count(op: int, dtype: int, m: int, n: int, k: int, ld: int = 0, axis: int = 0,
+                 accumulate: bool = False) -> int:
+    """Kernels one call of ``op`` enqueues for these sizes (see include/sq.h)."""
+    return int(load_library().sq_kernel_count(op, dtype, m, n, k, ld, axis, int(accumulate)))
 
 
 def calibrate_absmax(a: torch.Tensor, axis: int, out: torch.Tensor | None = None,
