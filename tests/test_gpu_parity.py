@@ -246,7 +246,14 @@ def test_gemm_saturated_widest_k(sq, codes):
 
 
 @pytest.mark.parametrize("codes", gemm_code_formats())
-@pytest.mark.parametrize("m,n,k", [(1, 8, 16), (1, 1, 4096), (17, 9, 48), (130, 257, 1040), (256, 256, 2048)])
+@pytest.mark.parametrize("m,n,k", [
+    (1, 8, 16), (1, 1, 4096), (17, 9, 48), (130, 257, 1040), (256, 256, 2048),
+    # tensor-core tile variants: CTA pairs with output-channel tiles of 128,
+    # 192, 224, 240 and 256 (chosen by the library per shape), a pair whose
+    # second CTA has no valid rows (M = 300), K tails inside a k-block and
+    # several 1024-product chunks
+    (129, 72, 80), (520, 3080, 272), (777, 3464, 1040), (777, 4040, 2064), (2048, 2168, 208),
+    (300, 1000, 3088)])
 def test_gemm_shapes_random_codes(sq, codes, m, n, k):
     u = synth.uniform(m + n + k, 5, (m + n) * k)
     codes_all = np.clip(np.floor(u * 255.0) - 127.0, -127, 127).astype(np.int8)

@@ -15,88 +15,95 @@
 // to int32 (exact) and add it to int32 running sums held in registers; the
 // MMA warp meanwhile fills the other of two TMEM accumulator buffers.
 //
-// Kernel shape: persistent, one CTA per SM, 128 x 256 output tiles,
-// 4-stage TMA pipeline of 128 x 64 (A) and 256 x 64 (B) bf16 tiles in
-// 128-byte-swizzled shared memory.  Warp 0 issues TMA loads, warp 1 owns
-// TMEM and issues the MMAs, warps 2-9 drain the accumulators and write Y.
-// Every mbarrier wait is bounded in time; a wait that runs out sets
-// SQ_FLAG_TIMEOUT, stops the CTA's loops, waits for its own outstanding
-// copies and MMAs (also bounded), frees TMEM and returns.
+// Kernel shape: persistent, 128 x 64 (A) and BN x 64 (B) bf16 tiles in
+// 128-byte-swizzled shared memory fed by a TMA pipeline.  Warp 0 issues TMA
+// loads, warp 1 owns TMEM and issues the MMAs, warps 2-9 drain the
+// accumulators and write Y.
+//   CG = 1: one CTA per SM computes 128 x BN output tiles.
+//   CG = 2: a cluster of two CTAs on two SMs computes 256 x BN tiles with
+//     tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of A and
+//     BN/2 rows of B, the even CTA issues M = 256 MMAs that read both CTAs'
+//     shared memory and write each CTA's own 128 accumulator lanes.  Per
+//     SM this moves 2/3 of the operand bytes of the one-CTA tile.
+// BN (the output-channel tile) is chosen per problem to fill the last wave
+// of tiles.  Every mbarrier wait is bounded in time; a wait that runs out
+// sets SQ_FLAG_TIMEOUT, stops the CTA's loops, waits (bounded) for its own
+// outstanding copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
-#include "sq_common.cuh"
+#include "sq_async.cuh"
 
 namespace sq {
 namespace tc {
+using async::su32;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128;       // accumulator lanes (rows of A) per CTA
+constexpr int BK = 64;        // 64 bf16 = one 128-byte swizzle row along K
 constexpr int CHUNK_KB = 16;  // k-blocks of 64 per exact fp32 chunk (1024 products)
-constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BYTES = BM * BK * 2;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = (2 + EPI_WARPS) * 32;
-constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulator buffers
-constexpr int COLS_PER_EPI_WARP = BN / 2;
-// instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t TMEM_COLS = 512;    // two accumulator buffers at columns 0 and 256
+constexpr uint32_t TMEM_BUF_STRIDE = 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
+template <int CG, int BN>
+struct Cfg {
+  static constexpr int B_ROWS = BN / CG;                 // rows of B this CTA loads
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // this CTA's bytes per stage
+  static constexpr int STAGES = (CG == 1 && BN > 128) ? 4 : 6;
+  static constexpr int MMA_M = BM * CG;
+  // instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+  // (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
+  static constexpr int COLS = BN / 2;  // accumulator columns per epilogue warp
+  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N");
+  static_assert(B_ROWS % 8 == 0, "whole 8-row swizzle atoms");
+  static_assert(COLS % 8 == 0, "epilogue works in 8-column groups");
+};
+
+template <int CG, int BN>
 struct Smem {
-  uint8_t a[STAGES][A_BYTES];
-  uint8_t b[STAGES][B_BYTES];
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  using C = Cfg<CG, BN>;
+  uint8_t a[C::STAGES][A_BYTES];
+  uint8_t b[C::STAGES][C::B_BYTES];
+  uint64_t full[C::STAGES];
+  uint64_t empty[C::STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + alignment slack
 
 // ------------------------------------------------------------------ PTX wrappers
-SQ_DEVINL uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+SQ_DEVINL void mbar_init(uint64_t* b, uint32_t count) { async::mbar_init(b, count); }
+SQ_DEVINL void mbar_expect_tx(uint64_t* b, uint32_t bytes) { async::mbar_expect_tx(b, bytes); }
+SQ_DEVINL bool mbar_try_wait(uint64_t* b, uint32_t parity) { return async::mbar_try_wait(b, parity); }
+SQ_DEVINL uint64_t global_ns() { return async::global_ns(); }
 
-SQ_DEVINL void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's
+// or the peer's).
+SQ_DEVINL void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
-SQ_DEVINL void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
-               : "memory");
-}
-SQ_DEVINL void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-SQ_DEVINL bool mbar_try_wait(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-SQ_DEVINL uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+
 // Bounded wait for the phase with parity `parity` to complete.  Returns
 // false if the CTA is aborting or the wait ran out (which starts the abort).
-SQ_DEVINL bool mbar_wait(uint64_t* b, uint32_t parity, Smem& sm, int32_t* flags,
+SQ_DEVINL bool mbar_wait(uint64_t* b, uint32_t parity, int* abort_flag, int32_t* flags,
                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(b, parity)) return true;
     if ((i & 63) == 0) {
-      if (*(volatile int*)&sm.abort) return false;
+      if (*(volatile int*)abort_flag) return false;
       if (global_ns() - t0 > limit_ns) {
-        *(volatile int*)&sm.abort = 1;
+        *(volatile int*)abort_flag = 1;
         raise_flag(flags, SQ_FLAG_TIMEOUT);
         return false;
       }
@@ -104,12 +111,24 @@ SQ_DEVINL bool mbar_wait(uint64_t* b, uint32_t parity, Smem& sm, int32_t* flags,
   }
 }
 
-SQ_DEVINL void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
-      "{%2, %3}], [%4];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
-      : "memory");
+// TMA load of box (x, y) into this CTA's shared memory, completing on the
+// mbarrier at shared::cluster address `bar` (with CG = 2, the even CTA's
+// barrier, which counts both CTAs' bytes).
+template <int CG>
+SQ_DEVINL void tma_load(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  if constexpr (CG == 2) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+        "[%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+  }
 }
 
 SQ_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -126,32 +145,74 @@ SQ_DEVINL uint64_t sw128_desc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-SQ_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
-      : "memory");
-}
-SQ_DEVINL void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   su32(bar))
-               : "memory");
+template <int CG>
+SQ_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                        uint32_t accumulate) {
+  if constexpr (CG == 2) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
-#define SQ_R32(i) "=r"(r[i])
-SQ_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : SQ_R32(0), SQ_R32(1), SQ_R32(2), SQ_R32(3), SQ_R32(4), SQ_R32(5), SQ_R32(6), SQ_R32(7),
-        SQ_R32(8), SQ_R32(9), SQ_R32(10), SQ_R32(11), SQ_R32(12), SQ_R32(13), SQ_R32(14), SQ_R32(15),
-        SQ_R32(16), SQ_R32(17), SQ_R32(18), SQ_R32(19), SQ_R32(20), SQ_R32(21), SQ_R32(22),
-        SQ_R32(23), SQ_R32(24), SQ_R32(25), SQ_R32(26), SQ_R32(27), SQ_R32(28), SQ_R32(29),
-        SQ_R32(30), SQ_R32(31)
-      : "r"(taddr));
+// Arrive (once) on `bar` when every MMA this thread issued so far has
+// completed; with CG = 2 on the barrier at the same offset in both CTAs.
+template <int CG>
+SQ_DEVINL void mma_commit(uint64_t* bar) {
+  if constexpr (CG == 2) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(su32(bar)),
+        "h"(mask)
+        : "memory");
+  } else {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     su32(bar))
+                 : "memory");
+  }
 }
-#undef SQ_R32
+
+template <int CG>
+SQ_DEVINL void tmem_alloc(uint32_t* dst) {
+  if constexpr (CG == 2) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(dst)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(dst)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+}
+
+template <int CG>
+SQ_DEVINL void tmem_dealloc(uint32_t taddr) {
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS)
+                 : "memory");
+}
+
+// 8 consecutive fp32 accumulator columns of this warp's 32 lanes.
+SQ_DEVINL void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
 SQ_DEVINL void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 SQ_DEVINL int32_t f32_to_i32_exact(uint32_t bits) {
@@ -167,99 +228,117 @@ struct Problem {
 };
 
 // ------------------------------------------------------------------ kernel
+template <int CG, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_bf16c(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const float* __restrict__ x_scale, const float* __restrict__ w_scale,
                  __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out, int32_t* flags,
                  Problem P) {
+  using C = Cfg<CG, BN>;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<CG, BN>& sm =
+      *reinterpret_cast<Smem<CG, BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? async::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;  // CTA pairs (CG = 2) or CTAs
   const int num_tiles = P.tiles_m * P.tiles_n;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.acc_full[b], 1);
-      mbar_init(&sm.acc_empty[b], EPI_WARPS);
+      mbar_init(&sm.acc_empty[b], EPI_WARPS * CG);
     }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+    async::fence_mbar_init();
+    async::prefetch_tensormap(&map_a);
+    async::prefetch_tensormap(&map_b);
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     su32(&sm.tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 1) tmem_alloc<CG>(&sm.tmem_base);
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    async::cluster_arrive();  // barriers initialised in both CTAs before any remote use
+    async::cluster_wait();
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // the even CTA's barriers, as shared::cluster addresses
+  const uint32_t full0 = CG == 2 ? async::mapa(su32(&sm.full[0]), 0) : su32(&sm.full[0]);
+  const uint32_t acc_empty0 = CG == 2 ? async::mapa(su32(&sm.acc_empty[0]), 0) : su32(&sm.acc_empty[0]);
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer (both CTAs load their own halves)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m0 = (tile % P.tiles_m) * BM, n0 = (tile / P.tiles_m) * BN;
+      for (int tile = unit; ok && tile < num_tiles; tile += n_units) {
+        const int m0 = (tile % P.tiles_m) * C::MMA_M + (int)rank * BM;
+        const int n0 = (tile / P.tiles_m) * BN + (int)rank * C::B_ROWS;
         for (int kb = 0; kb < P.n_kb; ++kb) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm, flags)) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1, &sm.abort, flags)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&sm.full[stage], STAGE_BYTES);
-          tma_load_2d(sm.a[stage], &map_a, &sm.full[stage], kb * BK, m0);
-          tma_load_2d(sm.b[stage], &map_b, &sm.full[stage], kb * BK, n0);
+          if (leader) mbar_expect_tx(&sm.full[stage], C::STAGE_BYTES * CG);
+          const uint32_t fb = full0 + stage * 8;
+          tma_load<CG>(sm.a[stage], &map_a, fb, kb * BK, m0);
+          tma_load<CG>(sm.b[stage], &map_b, fb, kb * BK, n0);
           ++issued;
-          if (++stage == STAGES) {
+          if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
       if (!ok) {
-        // let the copies already issued land before the CTA exits
-        for (int i = 0; i < STAGES && issued > 0; ++i, --issued) {
-          if (--stage < 0) {
-            stage = STAGES - 1;
-            phase ^= 1;
+        if (leader) {
+          // let the copies this pair issued land before the CTA exits
+          for (int i = 0; i < C::STAGES && issued > 0; ++i, --issued) {
+            if (--stage < 0) {
+              stage = C::STAGES - 1;
+              phase ^= 1;
+            }
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(&sm.full[stage], phase) && global_ns() - t0 < 10000000ull) {
+            }
           }
-          uint64_t t0 = global_ns();
-          while (!mbar_try_wait(&sm.full[stage], phase) && global_ns() - t0 < 10000000ull) {
+        } else {
+          // this CTA's copies complete on the even CTA's barriers: give them
+          // a bounded grace period instead
+          const uint64_t t0 = global_ns();
+          while (global_ns() - t0 < 10000000ull) {
           }
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
+    // ---------------- MMA issuer (the even CTA issues for the pair)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t chunk_ctr = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = unit; ok && tile < num_tiles; tile += n_units) {
         for (int c = 0; ok && c < P.n_chunks; ++c) {
           const uint32_t buf = chunk_ctr & 1, use = chunk_ctr >> 1;
-          if (!mbar_wait(&sm.acc_empty[buf], (use & 1) ^ 1, sm, flags)) {
+          if (!mbar_wait(&sm.acc_empty[buf], (use & 1) ^ 1, &sm.abort, flags)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem + buf * BN;
+          const uint32_t d = tmem + buf * TMEM_BUF_STRIDE;
           const int kb0 = c * CHUNK_KB, kb1 = min(P.n_kb, kb0 + CHUNK_KB);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&sm.full[stage], phase, sm, flags)) {
+            if (!mbar_wait(&sm.full[stage], phase, &sm.abort, flags)) {
               ok = false;
               break;
             }
@@ -267,43 +346,47 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t a_addr = su32(sm.a[stage]), b_addr = su32(sm.b[stage]);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                       (kb > kb0 || kk > 0) ? 1u : 0u);
-            mma_commit(&sm.empty[stage]);
-            if (++stage == STAGES) {
+              mma_bf16<CG>(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), C::IDESC,
+                           (kb > kb0 || kk > 0) ? 1u : 0u);
+            mma_commit<CG>(&sm.empty[stage]);
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1;
             }
           }
           if (!ok) break;
-          mma_commit(&sm.acc_full[buf]);
+          mma_commit<CG>(&sm.acc_full[buf]);
           ++chunk_ctr;
         }
       }
       // wait for every MMA this thread issued before TMEM is released
-      mma_commit(&sm.drain);
-      uint64_t t0 = global_ns();
+      asm volatile("tcgen05.commit.cta_group::%1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       su32(&sm.drain)),
+                   "n"(CG)
+                   : "memory");
+      const uint64_t t0 = global_ns();
       while (!mbar_try_wait(&sm.drain, 0) && global_ns() - t0 < WAIT_LIMIT_NS) {
       }
     }
   } else {
     // ---------------- epilogue warps: drain chunks, then write Y
-    const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;       // which 128 columns of the 256
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the BN columns
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t chunk_ctr = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const int64_t m0 = (int64_t)(tile % P.tiles_m) * BM, n0 = (int64_t)(tile / P.tiles_m) * BN;
-      int32_t acc[COLS_PER_EPI_WARP];
+    for (int tile = unit; ok && tile < num_tiles; tile += n_units) {
+      const int64_t m0 = (int64_t)(tile % P.tiles_m) * C::MMA_M + (int64_t)rank * BM;
+      const int64_t n0 = (int64_t)(tile / P.tiles_m) * BN;
+      int32_t acc[C::COLS];
 #pragma unroll
-      for (int i = 0; i < COLS_PER_EPI_WARP; ++i) acc[i] = 0;
+      for (int i = 0; i < C::COLS; ++i) acc[i] = 0;
       for (int c = 0; c < P.n_chunks; ++c) {
         const uint32_t buf = chunk_ctr & 1, use = chunk_ctr >> 1;
         // one lane waits and the warp follows its verdict, so the warp stays
         // converged for the .sync.aligned TMEM loads
         int got = 1;
-        if (lane == 0) got = mbar_wait(&sm.acc_full[buf], use & 1, sm, flags) ? 1 : 0;
+        if (lane == 0) got = mbar_wait(&sm.acc_full[buf], use & 1, &sm.abort, flags) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
         if (!got) {
           ok = false;
@@ -311,31 +394,38 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         tc_fence_after();
-        const uint32_t base = tmem + lane_base + buf * BN + half * COLS_PER_EPI_WARP;
+        const uint32_t base = tmem + lane_base + buf * TMEM_BUF_STRIDE + half * C::COLS;
 #pragma unroll
-        for (int j = 0; j < COLS_PER_EPI_WARP / 64; ++j) {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(base + j * 64, r0);
-          tmem_ld32(base + j * 64 + 32, r1);
+        for (int j = 0; j < C::COLS / 8; j += 2) {
+          uint32_t r[2][8];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (j + u < C::COLS / 8) tmem_ld8(base + (j + u) * 8, r[u]);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            acc[j * 64 + i] += f32_to_i32_exact(r0[i]);
-            acc[j * 64 + 32 + i] += f32_to_i32_exact(r1[i]);
-          }
+          for (int u = 0; u < 2; ++u)
+            if (j + u < C::COLS / 8) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[(j + u) * 8 + i] += f32_to_i32_exact(r[u][i]);
+            }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            mbar_arrive_cluster(acc_empty0 + buf * 8);
+          else
+            async::mbar_arrive_local(&sm.acc_empty[buf]);
+        }
         ++chunk_ctr;
       }
       if (!ok) break;
       const int64_t m = m0 + q * 32 + lane;
       if (m < P.M) {
         const float xs = x_scale[m];
-        const int64_t nb = n0 + half * COLS_PER_EPI_WARP;
+        const int64_t nb = n0 + half * C::COLS;
 #pragma unroll
-        for (int g = 0; g < COLS_PER_EPI_WARP / 8; ++g) {
+        for (int g = 0; g < C::COLS / 8; ++g) {
           const int64_t n = nb + g * 8;
           if (n >= P.N) break;
           float v[8];
@@ -376,32 +466,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    // the peer may still touch this CTA's barriers and TMEM until both
+    // CTAs are here
+    async::cluster_arrive();
+    async::cluster_wait();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
-                 : "memory");
+    tmem_dealloc<CG>(tmem);
   }
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // 2-D bf16 tensor [rows x k] (k contiguous), box of 64 x box_rows, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint32_t box_rows) {
-  auto fn = encode_fn();
+  auto fn = async::tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)k * 2};
@@ -413,19 +496,18 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint3
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace tc
-
-sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
-                        int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
-                        cudaStream_t st) {
-  using namespace tc;
-  if (m > (int64_t)1 << 31 || n > (int64_t)1 << 31 || k > (int64_t)1 << 31) return SQ_ERR_UNSUPPORTED;
+template <int CG, int BN>
+sq_status launch(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
+                 int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
+                 cudaStream_t st) {
+  using C = Cfg<CG, BN>;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, xq, m, k, BM) || !make_map(&mb, wq, n, k, BN)) return SQ_ERR_CUDA;
+  if (!make_map(&ma, xq, m, k, BM) || !make_map(&mb, wq, n, k, C::B_ROWS)) return SQ_ERR_CUDA;
+  auto kern = k_gemm_bf16c<CG, BN>;
+  const size_t smem = sizeof(Smem<CG, BN>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(k_gemm_bf16c, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return SQ_ERR_CUDA;
     attr_set = true;
   }
@@ -433,16 +515,70 @@ sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, co
   P.M = m;
   P.N = n;
   P.K = k;
-  P.tiles_m = (int)((m + BM - 1) / BM);
+  P.tiles_m = (int)((m + C::MMA_M - 1) / C::MMA_M);
   P.tiles_n = (int)((n + BN - 1) / BN);
   P.n_kb = (int)((k + BK - 1) / BK);
   P.n_chunks = (P.n_kb + CHUNK_KB - 1) / CHUNK_KB;
   P.vec_ok = (n % 8 == 0) && aligned16(y) && (acc_out == nullptr || aligned16(acc_out));
   const int tiles = P.tiles_m * P.tiles_n;
-  const int grid = std::min(tiles, sm_count());
-  k_gemm_bf16c<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, x_scale, w_scale,
-                                                   static_cast<__nv_bfloat16*>(y), acc_out, flags, P);
+  const int units = std::min(tiles, sm_count() / CG);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units * CG), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, ma, mb, x_scale, w_scale, static_cast<__nv_bfloat16*>(y),
+                         acc_out, flags, P) != cudaSuccess)
+    return SQ_ERR_CUDA;
   return launch_status();
+}
+
+// Output-channel tile for a CTA pair: the candidate whose whole waves of
+// tiles cost least, a tile's cost taken as its width plus a fixed overhead
+// of 16 columns.
+int choose_bn(int64_t m, int64_t n, int units, int mma_m) {
+  const int cand[] = {256, 240, 224, 192, 128};
+  const int64_t tiles_m = (m + mma_m - 1) / mma_m;
+  int best = 256;
+  int64_t best_cost = INT64_MAX;
+  for (int bn : cand) {
+    const int64_t tiles = tiles_m * ((n + bn - 1) / bn);
+    const int64_t waves = (tiles + units - 1) / units;
+    const int64_t cost = waves * (bn + 16);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+}  // namespace tc
+
+// Tiles of 256 rows (CTA pairs) once M exceeds one 128-row tile.
+int gemm_bf16c_cta_group(int64_t m) { return m > tc::BM ? 2 : 1; }
+
+sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
+                        int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
+                        cudaStream_t st) {
+  using namespace tc;
+  if (m > (int64_t)1 << 31 || n > (int64_t)1 << 31 || k > (int64_t)1 << 31) return SQ_ERR_UNSUPPORTED;
+  if (gemm_bf16c_cta_group(m) == 1)
+    return launch<1, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+  switch (choose_bn(m, n, sm_count() / 2, 2 * BM)) {
+    case 240: return launch<2, 240>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+    case 224: return launch<2, 224>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+    case 192: return launch<2, 192>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+    case 128: return launch<2, 128>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+    default: return launch<2, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+  }
 }
 
 }  // namespace sq

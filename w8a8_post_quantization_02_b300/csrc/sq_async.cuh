@@ -28,6 +28,10 @@ SQ_DEVINL void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
                : "memory");
 }
 
+SQ_DEVINL void mbar_arrive_local(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+
 SQ_DEVINL bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
