@@ -25,7 +25,7 @@ blocking or reordering.  Sources (page title, then the passage):
 * learn-kernels.com "Quantization", paragraph 2: both operands of the
   matmul quantized to INT8, the transform applied offline before serving.
 
-Readings where the pages are silent (all listed in the design doc as well):
+Readings where the pages are silent:
 
 1. general smoothing strength: s_j = max|X_j|^a / max|W_j|^(1-a); a = 0.5
    is the printed case.  Each power is the correctly rounded binary32

@@ -248,10 +248,10 @@ def test_gemm_saturated_widest_k(sq, codes):
 @pytest.mark.parametrize("codes", gemm_code_formats())
 @pytest.mark.parametrize("m,n,k", [
     (1, 8, 16), (1, 1, 4096), (17, 9, 48), (130, 257, 1040), (256, 256, 2048),
-    # tensor-core tile variants: CTA pairs with output-channel tiles of 128,
-    # 192, 224, 240 and 256 (chosen by the library per shape), a pair whose
-    # second CTA has no valid rows (M = 300), K tails inside a k-block and
-    # several 1024-product chunks
+    # tensor-core tiles: CTA pairs with output-channel tiles of 240 and 256
+    # (chosen by the library per shape), a pair whose second CTA has no
+    # valid rows (M = 300), K tails inside a k-block and several
+    # 1024-product chunks
     (129, 72, 80), (520, 3080, 272), (777, 3464, 1040), (777, 4040, 2064), (2048, 2168, 208),
     (300, 1000, 3088)])
 def test_gemm_shapes_random_codes(sq, codes, m, n, k):
@@ -269,13 +269,14 @@ def test_gemm_shapes_random_codes(sq, codes, m, n, k):
 
 # ------------------------------------------------------------------ launch-shape coverage
 # Weight shapes that reach every single-pass fold configuration: clusters of
-# 1, 2, 4 and 8 CTAs (Cin up to 1536, 3072, 6144, 12288 rows), a cluster
-# whose last CTA owns no rows (Cin = 6160 with 8 x 896-row CTAs), strips cut
-# short by Cout, fp32 weights, and Cin beyond the single-pass limit (the
-# two-pass path).
+# 1, 2, 4 and 8 CTAs of at most 1536 rows (Cin up to 1536, 3072, 6144,
+# 12288), a cluster whose last CTA owns no rows (Cin = 6160 with 8 x
+# 896-row CTAs), strips cut short by Cout, fp32 weights, and Cin beyond the
+# single-pass limit (the two-pass path).
 FOLD_SHAPES = [
-    (1536, 96, "bf16"), (1552, 40, "bf16"), (4096, 264, "bf16"), (6160, 72, "bf16"),
-    (12288, 32, "bf16"), (12304, 24, "bf16"), (2048, 20, "f32"), (48, 1000, "f32"),
+    (768, 40, "bf16"), (1536, 96, "bf16"), (1552, 40, "bf16"), (4096, 264, "bf16"),
+    (6160, 72, "bf16"), (12288, 32, "bf16"), (12304, 24, "bf16"), (2048, 20, "f32"),
+    (48, 1000, "f32"),
 ]
 
 
@@ -321,12 +322,13 @@ def test_quant_act_launch_shapes(sq, tokens, cin, dtype, codes):
 
 
 # Column-maxima shapes for the strip kernel: clusters of 1-8 CTAs, a last
-# CTA with a partial box, a strip cut short by the column count, running
-# maxima over two batches, and a row stride that is not 16-byte aligned
-# (the atomic path).
+# CTA with a partial box, strips cut short by the column count, rings that
+# wrap many times (5000 rows), wide rows, running maxima over two batches,
+# and a row stride that is not 16-byte aligned (the atomic path).
 COLMAX_SHAPES = [
     (16, 4096, "bf16"), (2048, 4096, "bf16"), (300, 64, "bf16"), (1000, 40, "f32"),
-    (129, 528, "f32"), (5000, 96, "bf16"), (77, 300, "bf16"),
+    (129, 528, "f32"), (5000, 96, "bf16"), (77, 300, "bf16"), (3, 4096, "bf16"),
+    (40, 32768, "bf16"), (24, 12288, "f32"), (6, 40000, "bf16"),
 ]
 
 

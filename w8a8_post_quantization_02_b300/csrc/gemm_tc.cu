@@ -25,8 +25,8 @@
 //     BN/2 rows of B, the even CTA issues M = 256 MMAs that read both CTAs'
 //     shared memory and write each CTA's own 128 accumulator lanes.  Per
 //     SM this moves 2/3 of the operand bytes of the one-CTA tile.
-// BN (the output-channel tile) is chosen per problem to fill the last wave
-// of tiles.  Every mbarrier wait is bounded in time; a wait that runs out
+// BN (the output-channel tile, 256 or 240) is chosen per problem to fill
+// the last wave of tiles.  Every mbarrier wait is bounded in time; a wait that runs out
 // sets SQ_FLAG_TIMEOUT, stops the CTA's loops, waits (bounded) for its own
 // outstanding copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -540,24 +540,20 @@ sq_status launch(const void* xq, const float* x_scale, const void* wq, const flo
   return launch_status();
 }
 
-// Output-channel tile for a CTA pair: the candidate whose whole waves of
-// tiles cost least, a tile's cost taken as its width plus a fixed overhead
-// of 16 columns.
+// Output-channel tile for a CTA pair, 256 or 240.  Measured on B300 with
+// the prefill, down_proj and Q/K/V workloads: narrower MMAs (N = 224, 192,
+// 128) take nearly as long per instruction as N = 256, and a 240-wide tile
+// takes about 0.985 of a 256-wide one.  The cost below is the per-pair
+// time of the busiest pair (whole waves of tiles) plus 0.3 x the average
+// load, which orders the three measured shapes correctly.
 int choose_bn(int64_t m, int64_t n, int units, int mma_m) {
-  const int cand[] = {256, 240, 224, 192, 128};
   const int64_t tiles_m = (m + mma_m - 1) / mma_m;
-  int best = 256;
-  int64_t best_cost = INT64_MAX;
-  for (int bn : cand) {
+  auto cost = [&](int bn, double t) {
     const int64_t tiles = tiles_m * ((n + bn - 1) / bn);
     const int64_t waves = (tiles + units - 1) / units;
-    const int64_t cost = waves * (bn + 16);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = bn;
-    }
-  }
-  return best;
+    return (double)waves * t + 0.3 * (double)tiles * t / units;
+  };
+  return cost(240, 0.985) < cost(256, 1.0) ? 240 : 256;
 }
 
 }  // namespace tc
@@ -572,13 +568,9 @@ sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, co
   if (m > (int64_t)1 << 31 || n > (int64_t)1 << 31 || k > (int64_t)1 << 31) return SQ_ERR_UNSUPPORTED;
   if (gemm_bf16c_cta_group(m) == 1)
     return launch<1, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
-  switch (choose_bn(m, n, sm_count() / 2, 2 * BM)) {
-    case 240: return launch<2, 240>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
-    case 224: return launch<2, 224>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
-    case 192: return launch<2, 192>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
-    case 128: return launch<2, 128>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
-    default: return launch<2, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
-  }
+  if (choose_bn(m, n, sm_count() / 2, 2 * BM) == 240)
+    return launch<2, 240>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+  return launch<2, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
 }
 
 }  // namespace sq

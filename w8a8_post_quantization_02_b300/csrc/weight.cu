@@ -367,7 +367,8 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
   if constexpr (CL > 1) cluster_arrive();  // done reading the peers' shared memory
   __syncthreads();
 
-  // ---- pass 2: codes of 8 consecutive rows x one chunk per thread
+  // ---- pass 2: codes of 8 consecutive rows x one chunk per thread, in
+  // two halves of 4 rows packed as they are produced (few live registers)
   {
     const int c = tid & 3;
     const bool clamp = *clamp_flag != 0;
@@ -375,22 +376,40 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
 #pragma unroll
     for (int e = 0; e < EPC; ++e) inv[e] = inv_sm[c * EPC + e];
     for (int g = tid >> 2; g * 8 < rows; g += kThreads / 4) {
-      float q[8][EPC];
+      constexpr int WPC = CODES == SQ_CODES_BF16 ? 4 : 2;  // 32-bit words per channel
+      uint32_t out[EPC][WPC];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int r = g * 8 + k;
-        unpack_chunk<BF16>(*reinterpret_cast<const uint4*>(strip + chunk_off(r, c)), q[k]);
-        const float sj = s_sm[r];
+      for (int h = 0; h < 2; ++h) {
+        float q[4][EPC];
 #pragma unroll
-        for (int e = 0; e < EPC; e += 2) mul2_rn(q[k][e], q[k][e + 1], sj, sj);
-        if (!clamp) {
-          // scalar multiply then add (never contracted into a fused
-          // multiply-add, which would round ties differently)
+        for (int k = 0; k < 4; ++k) {
+          const int r = g * 8 + h * 4 + k;
+          unpack_chunk<BF16>(*reinterpret_cast<const uint4*>(strip + chunk_off(r, c)), q[k]);
+          const float sj = s_sm[r];
 #pragma unroll
-          for (int e = 0; e < EPC; ++e) q[k][e] = __fadd_rn(__fmul_rn(q[k][e], inv[e]), kMagic);
-        } else {
+          for (int e = 0; e < EPC; e += 2) mul2_rn(q[k][e], q[k][e + 1], sj, sj);
+          if (!clamp) {
+            // scalar multiply then add (never contracted into a fused
+            // multiply-add, which would round ties differently)
 #pragma unroll
-          for (int e = 0; e < EPC; ++e) q[k][e] = code_magic(q[k][e], inv[e]);
+            for (int e = 0; e < EPC; ++e) q[k][e] = __fadd_rn(__fmul_rn(q[k][e], inv[e]), kMagic);
+          } else {
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) q[k][e] = code_magic(q[k][e], inv[e]);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) {
+          if constexpr (CODES == SQ_CODES_BF16) {
+#pragma unroll
+            for (int k = 0; k < 4; k += 2) {
+              float c0 = q[k][e], c1 = q[k + 1][e];
+              add2_rn(c0, c1, -kMagic, -kMagic);  // exact integers
+              out[e][h * 2 + k / 2] = __byte_perm(__float_as_uint(c0), __float_as_uint(c1), 0x7632);
+            }
+          } else {
+            out[e][h] = pack4_codes(q[0][e], q[1][e], q[2][e], q[3][e]);
+          }
         }
       }
       const int64_t jrow = j0 + (int64_t)g * 8;
@@ -399,19 +418,10 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
         const int64_t n = n0 + c * EPC + e;
         if (n >= cout) continue;
         uint8_t* dst = wq + (n * cin + jrow) * CB;
-        if constexpr (CODES == SQ_CODES_BF16) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int k = 0; k < 8; k += 2) {
-            float c0 = q[k][e], c1 = q[k + 1][e];
-            add2_rn(c0, c1, -kMagic, -kMagic);  // exact integers
-            w4[k / 2] = __byte_perm(__float_as_uint(c0), __float_as_uint(c1), 0x7632);
-          }
-          st16(dst, make_uint4(w4[0], w4[1], w4[2], w4[3]));
-        } else {
-          st8(dst, make_uint2(pack4_codes(q[0][e], q[1][e], q[2][e], q[3][e]),
-                              pack4_codes(q[4][e], q[5][e], q[6][e], q[7][e])));
-        }
+        if constexpr (CODES == SQ_CODES_BF16)
+          st16(dst, make_uint4(out[e][0], out[e][1], out[e][2], out[e][3]));
+        else
+          st8(dst, make_uint2(out[e][0], out[e][1]));
       }
     }
   }
@@ -438,7 +448,8 @@ sq_status launch(const CUtensorMap& map, const float* s, int64_t cin, int64_t co
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<EPC>(kMaxRows).total + 1024) != cudaSuccess)
+                             (int)Layout<EPC>(kMaxRows).total + 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return SQ_ERR_CUDA;
     attr_done = true;
   }
