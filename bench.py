@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--act-scale", choices=["dynamic", "static"], default="dynamic",
+                    help="per-token scales (default) or one calibrated scale per tensor")
     return ap.parse_args()
 
 
@@ -243,7 +245,7 @@ def run_ours(args, case_name):
     peaks, peaks_kind = load_peaks()
     case = synth.workload(case_name)
     x_host, w_host = to_device(case, torch)
-    layer = pipeline.Layer.for_case(case)
+    layer = pipeline.Layer.for_case(case, act_scale=args.act_scale)
     layer.load(x_host.cuda(), w_host.cuda())
     stream = torch.cuda.current_stream()
     st = sq._stream(stream)
@@ -311,6 +313,7 @@ def run_ours(args, case_name):
         gbs = nbytes[name] / (us * 1e-6) / 1e9
         iso[name] = {"us": round(us, 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
     iso["gemm"]["tops"] = round(ops / (iso["gemm"]["us"] * 1e-6) / 1e12, 2)
+    act_stage = "quant_act" if args.act_scale == "dynamic" else "quant_act_static"
 
     bf16_peak = float(peaks["bf16_tflops"])
     if layer.codes == "bf16":
@@ -332,10 +335,10 @@ def run_ours(args, case_name):
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "s8", "data": "synthetic",
-        "config": workload_config(case, layer.codes),
+        "config": dict(workload_config(case, layer.codes), act_scale=args.act_scale),
         "gemm_tops": gemm_tops,
-        "act_quant_gbs": iso["quant_act"]["gbs"],
-        "act_quant_hbm_frac": iso["quant_act"]["hbm_frac"],
+        "act_quant_gbs": iso[act_stage]["gbs"],
+        "act_quant_hbm_frac": iso[act_stage]["hbm_frac"],
         "stages_isolated": iso,
         "roofline": roofline,
         "gpu_launches": launches,

@@ -74,7 +74,9 @@ typedef enum {
   SQ_OP_SMOOTH = 1,
   SQ_OP_FOLD_QUANTIZE = 2,
   SQ_OP_QUANT_ACT = 3,
-  SQ_OP_GEMM = 4
+  SQ_OP_GEMM = 4,
+  SQ_OP_STATIC_SCALE = 5,
+  SQ_OP_QUANT_ACT_STATIC = 6
 } sq_op;
 
 /*
@@ -187,6 +189,36 @@ sq_status sq_quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, 
                        int32_t* dev_flags, cudaStream_t stream);
 
 /*
+ * Step 4, static variant - one calibrated activation scale per tensor.
+ * Source: SmoothQuant glossary (dataterminology.com): calibration-based,
+ * statistics from a small calibration set; first page, paragraph 3 (the
+ * runtime multiply by S^-1).  Two calls:
+ *
+ * sq_static_act_scale: from the calibration statistics of step 1 (amax_x,
+ * a running maximum over the calibration batches) and s_inv of step 2,
+ *   d = RN(max_j RN(amax_x[j] * s_inv[j]) / 127)   (1 if the maximum is 0)
+ * which is max|X'| / 127 over the calibration data (a binary32 multiply by
+ * a fixed positive factor is monotone in |x|).
+ *   amax_x, s_inv  device fp32 [cin];  d  device fp32 [1]
+ *   dev_flags      device int32 or NULL (SQ_FLAG_NONFINITE)
+ *
+ * sq_quant_act_static: X' = X * s_inv, codes with the one scale d:
+ *   xq[t,j] = clamp(rne(X'[t,j] * (1/d)), -127, 127);  x_scale[t] = d
+ * (x_scale is filled so that sq_w8a8_gemm's epilogue is unchanged).  Values
+ * beyond the calibration maximum saturate; `clipped` (device uint32 or
+ * NULL) has the number of elements the clamp changed ADDED to it.  A NaN in
+ * X' gives code 0 and +-inf saturates; both raise SQ_FLAG_NONFINITE.  A
+ * single streaming pass with no per-token reduction.  Layout and
+ * alignment as sq_quant_act; d is read on the device.
+ */
+sq_status sq_static_act_scale(const float* amax_x, const float* s_inv, int64_t cin, float* d,
+                              int32_t* dev_flags, cudaStream_t stream);
+sq_status sq_quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                              const float* s_inv, const float* d, void* xq, sq_codes fmt,
+                              float* x_scale, uint32_t* clipped, int32_t* dev_flags,
+                              cudaStream_t stream);
+
+/*
  * Step 5 - INT8 x INT8 GEMM with exact integer accumulation and a bf16
  * dequantizing epilogue.
  * Source: learn-kernels.com "Quantization", paragraph 2 (the matmul runs on
@@ -209,6 +241,46 @@ sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq,
                        const float* w_scale, sq_codes fmt, int64_t m, int64_t n, int64_t k,
                        void* y, int32_t* acc_out, int32_t* dev_flags, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Diagnostics - the second half of the validation order.
+ * Source: first page, paragraph 4 (after the unquantized rewrite, quantize
+ * and measure activation clipping and weight reconstruction separately);
+ * Smooth Rotation review, referee report (layer-wise squared Frobenius
+ * quantization error; "quantization difficulty" = standard deviation of
+ * channel magnitudes).  Differences x - code * scale are exact in float64;
+ * squares and sums are rounded in float64 (order-dependent in the last
+ * bits).  None of these is on the timed path.
+ *
+ * sq_act_quant_error: err[t] = sum_j (RN(X[t,j] * s_inv[j]) - xq[t,j] * x_scale[t])^2
+ *   x, s_inv, xq, x_scale as sq_quant_act (same layouts and alignment);
+ *   err device double [tokens].
+ * sq_weight_quant_error: err[n] = sum_j (RN(s[j] * W[j,n]) - wq[n,j] * w_scale[n])^2
+ *   w, s, wq, w_scale as sq_fold_quantize_weight (any row alignment);
+ *   err device double [cout].
+ * sq_layer_error: for the sampled tokens rows[0..nrows),
+ *   err[r] = sum_n ((X W)[rows[r], n] - y[rows[r], n])^2
+ *   with X W formed from the unquantized inputs (fp32 chunks of 32 products
+ *   summed in float64; relative error ~1e-6 of |X W|).  x [tokens x cin]
+ *   (ldx), w [cin x cout] (ldw), both of type dt; y bf16 [tokens x cout]
+ *   contiguous; rows device int32 [nrows], 1 <= nrows <= 64; err device
+ *   double [nrows] (overwritten).
+ * sq_channel_stats: out[0] = mean, out[1] = population standard deviation
+ *   of v_j = RN(amax[j] * scale[j]) (scale NULL: v_j = amax[j]); with
+ *   amax = max|X_j| and scale = s_inv, the channel magnitudes after
+ *   smoothing.  out device double [2].
+ */
+sq_status sq_act_quant_error(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                             const float* s_inv, const void* xq, sq_codes fmt, const float* x_scale,
+                             double* err, cudaStream_t stream);
+sq_status sq_weight_quant_error(const void* w, sq_dtype dt, int64_t cin, int64_t cout, int64_t ldw,
+                                const float* s, const void* wq, sq_codes fmt, const float* w_scale,
+                                double* err, cudaStream_t stream);
+sq_status sq_layer_error(const void* x, const void* w, sq_dtype dt, int64_t tokens, int64_t cin,
+                         int64_t cout, int64_t ldx, int64_t ldw, const void* y,
+                         const int32_t* rows, int nrows, double* err, cudaStream_t stream);
+sq_status sq_channel_stats(const float* amax, const float* scale, int64_t n, double* out,
+                           cudaStream_t stream);
 
 /* Workspace bytes an operation needs for these sizes (0 if none). */
 size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fmt);

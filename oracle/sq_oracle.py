@@ -205,6 +205,54 @@ def quant_act(x, s_inv, return_scaled: bool = False):
 
 
 # --------------------------------------------------------------------------
+# step 4, static variant: one calibrated scale per activation tensor
+# --------------------------------------------------------------------------
+def static_act_scale(amax_x, s_inv):
+    """Per-tensor activation scale from the calibration statistics.
+
+    SmoothQuant glossary (dataterminology.com): the method is
+    calibration-based, its statistics come from a small calibration set.
+    Reading: the activation scale may be fixed from those statistics too,
+    d = max over the tensor of |X'| / 127 with X' = X * (1/s).  Because a
+    binary32 multiply by a fixed positive factor is monotone in |x|, the
+    largest |X'[t, j]| over tokens is RN(max_t |X[t, j]| * s_inv[j]), so d
+    follows from the per-channel maxima alone.  Returns ``(d, nonfinite)``.
+    """
+    ax = np.asarray(amax_x, dtype=F32)
+    si = np.asarray(s_inv, dtype=F32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        v = (ax * si).astype(F32)          # one binary32 multiply per channel
+    m = F32(np.max(v)) if v.size else F32(0)
+    if np.isnan(v).any():
+        m = F32(np.nan)
+    d, _, nonfinite = _scale_and_inverse(np.array([m], dtype=F32))
+    return F32(d[0]), nonfinite
+
+
+def quant_act_static(x, s_inv, d):
+    """X' = X * (1/s), codes with one fixed scale d for every token.
+
+    Same quantizer as ``quant_act`` (reading 4) with the per-token scale
+    replaced by the calibrated d: codes clamp(rne(X' * (1/d)), -127, 127).
+    Runtime activations may exceed the calibration maximum, so the clamp
+    can act; ``clipped`` counts the elements it changed.  Returns ``(xq,
+    x_scale, clipped)`` with x_scale = d for every token, so the GEMM's
+    epilogue is unchanged.
+    """
+    x32 = np.asarray(x, dtype=F32)
+    si = np.asarray(s_inv, dtype=F32)
+    d = F32(d)
+    inv = F32(F32(1.0) / d)
+    with np.errstate(over="ignore", invalid="ignore"):
+        xs = (x32 * si[None, :]).astype(F32)
+        t = (xs * inv).astype(F32)
+        r = np.rint(t)
+    clipped = int(np.count_nonzero(np.isfinite(r) & (np.abs(r) > QMAX)))
+    q = _codes(xs, np.full(xs.shape[0], inv, dtype=F32)[:, None])
+    return q, np.full(xs.shape[0], d, dtype=F32), clipped
+
+
+# --------------------------------------------------------------------------
 # step 5: INT8 x INT8 -> exact accumulators -> bf16 epilogue
 # --------------------------------------------------------------------------
 def int_accumulate(xq, wq, rows=None) -> np.ndarray:
@@ -274,6 +322,62 @@ def w8a8_gemm(xq, x_scale, wq, w_scale, rows=None):
 
 
 # --------------------------------------------------------------------------
+# diagnostics: the second half of the validation order
+# --------------------------------------------------------------------------
+F64 = np.float64
+
+
+def act_quant_error(x, s_inv, xq, x_scale):
+    """Per token: sum_j (X'[t, j] - xq[t, j] * x_scale[t])^2 in float64.
+
+    First page, paragraph 4: after the unquantized rewrite checks out,
+    quantize and measure activation error and clipping separately.  X' is
+    the binary32 X * (1/s) the quantizer saw; each difference is exact in
+    float64, the squares and the sum are rounded in float64.
+    """
+    xs = (np.asarray(x, F32) * np.asarray(s_inv, F32)[None, :]).astype(F32).astype(F64)
+    deq = np.asarray(xq).astype(F64) * np.asarray(x_scale, F32).astype(F64)[:, None]
+    return ((xs - deq) ** 2).sum(axis=1)
+
+
+def weight_quant_error(w, s, wq, w_scale):
+    """Per output channel: sum_j (W'[j, n] - wq[n, j] * w_scale[n])^2 in float64
+    (first page, paragraph 4: weight reconstruction error).  W' is the
+    binary32 fold s_j * W[j, n]."""
+    wf = (np.asarray(s, F32)[:, None] * np.asarray(w, F32)).astype(F32).astype(F64)
+    deq = np.asarray(wq).astype(F64).T * np.asarray(w_scale, F32).astype(F64)[None, :]
+    return ((wf - deq) ** 2).sum(axis=0)
+
+
+def layer_error(x, w, y_bits, rows):
+    """Per sampled token t: sum_n ((X W)[t, n] - Y[t, n])^2 in float64.
+
+    Smooth Rotation review (referee report summary): the layer-wise squared
+    Frobenius quantization error; here against the layer's bf16 output Y
+    (bit patterns of the whole [tokens x Cout] output; the rows listed are
+    used), with X W formed in float64 from the unquantized inputs.
+    """
+    rows = np.asarray(rows)
+    ref = np.asarray(x, F32)[rows].astype(F64) @ np.asarray(w, F32).astype(F64)
+    yb = np.asarray(y_bits, np.uint16)[rows]          # Y is the whole output [tokens x Cout]
+    y = (yb.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return ((ref - y.astype(F64)) ** 2).sum(axis=1)
+
+
+def channel_stats(amax, scale=None):
+    """(mean, population standard deviation) of the per-channel magnitudes
+    max|X_j| (times ``scale`` in binary32 when given, i.e. after smoothing).
+    Smooth Rotation review: "quantization difficulty" is the standard
+    deviation of channel magnitudes."""
+    v = np.asarray(amax, F32)
+    if scale is not None:
+        v = (v * np.asarray(scale, F32)).astype(F32)
+    v = v.astype(F64)
+    mean = v.sum() / v.size
+    return mean, float(np.sqrt(((v - mean) ** 2).sum() / v.size))
+
+
+# --------------------------------------------------------------------------
 # the whole path on one layer
 # --------------------------------------------------------------------------
 def run_path(x, w, alpha, rows=None):
@@ -299,6 +403,8 @@ def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
 
 __all__ = [
     "calibrate_absmax", "rn32_pow", "smooth_factors", "fold_quantize_weight", "quant_act",
+    "static_act_scale", "quant_act_static", "act_quant_error", "weight_quant_error",
+    "layer_error", "channel_stats",
     "int_accumulate", "bf16_rne_bits", "w8a8_gemm", "run_path", "bf16_ulp_distance",
     "STAT_FLOOR", "S_MIN", "S_MAX", "QMAX",
 ]

@@ -383,3 +383,157 @@ def test_full_workload_parity(sq, name):
     assert np.array_equal(layer.acc.index_select(0, rows_t).cpu().numpy().astype(np.int64), acc_ref)
     y = y_bits(layer.y.index_select(0, rows_t))
     assert O.bf16_ulp_distance(y, y_ref).max() <= 1
+
+
+# ------------------------------------------------------------------ static activation scale
+# Calibrate on X, then quantize a runtime batch whose tokens are scaled by
+# up to 1.6x (so some codes clip): scale, codes and clip count bit-exact.
+STATIC_SHAPES = [
+    (64, 512, "f32"), (37, 80, "bf16"), (300, 11008, "bf16"), (9, 16384, "f32"), (4099, 64, "bf16"),
+    (700, 4112, "bf16"), (1, 256, "bf16"),
+]
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+@pytest.mark.parametrize("tokens,cin,dtype", STATIC_SHAPES)
+def test_static_scale_and_codes_bit_exact(sq, tokens, cin, dtype, codes):
+    c = synth.make_case("st", tokens, cin, 16, dtype=dtype, outlier_frac=0.02, seed=tokens + 3 * cin)
+    cal = c.x_f32()
+    si = (0.25 + 4.0 * synth.uniform(cin, 43, cin)).astype(F32)
+    ax = O.calibrate_absmax(cal, 0)
+    d_ref, nf = O.static_act_scale(ax, si)
+    flags = flags_tensor()
+    d = sq.static_act_scale(torch.from_numpy(ax).cuda(), torch.from_numpy(si).cuda(), flags)
+    assert f32bits(d)[0] == npbits([d_ref])[0] and not nf
+    gain = (1.0 + 0.6 * synth.uniform(tokens, 44, tokens)).astype(F32)
+    run = (cal * gain[:, None]).astype(F32)
+    if dtype == "bf16":
+        bits = synth.f64_to_bf16_bits(run.astype(np.float64))
+        run = synth.bf16_bits_to_f32(bits)
+        run_dev = dev(bits, "bf16")
+    else:
+        run_dev = dev(run, "f32")
+    q_ref, xs_ref, clip_ref = O.quant_act_static(run, si, d_ref)
+    clipped = torch.zeros(1, dtype=torch.int32, device="cuda")
+    xq, xs = sq.quant_act_static(run_dev, torch.from_numpy(si).cuda(), d, codes, clipped, flags)
+    assert int(flags.item()) == 0
+    assert np.array_equal(codes_np(xq), q_ref)
+    assert np.array_equal(f32bits(xs), npbits(xs_ref))
+    assert int(clipped.item()) == clip_ref
+
+
+def test_static_nonfinite_codes_and_flag(sq):
+    x = torch.ones(3, 32, device="cuda")
+    x[1, 5] = float("nan")
+    x[2, 7] = float("inf")
+    x[2, 8] = -float("inf")
+    d = torch.tensor([1.0 / 127.0], device="cuda")
+    flags, clipped = flags_tensor(), torch.zeros(1, dtype=torch.int32, device="cuda")
+    xq, _ = sq.quant_act_static(x, torch.ones(32, device="cuda"), d, "i8", clipped, flags)
+    q = codes_np(xq)
+    assert int(flags.item()) & 1
+    assert q[1, 5] == 0 and q[2, 7] == 127 and q[2, 8] == -127
+    ref, _, clip_ref = O.quant_act_static(x.cpu().numpy(), np.ones(32, F32), F32(1.0 / 127.0))
+    assert np.array_equal(q, ref) and int(clipped.item()) == clip_ref
+
+
+@pytest.mark.parametrize("name", ["prefill_upgate_2048x4096x11008", "qkv_shared_8192x8192x10240"])
+def test_full_workload_static_parity(sq, name):
+    from w8a8_post_quantization_02_b300 import pipeline
+    c = synth.workload(name)
+    ax = O.calibrate_absmax(c.x_f32(), 0)
+    s_ref, si_ref, _ = O.smooth_factors(ax, O.calibrate_absmax(c.w_f32(), 1), c.alpha)
+    d_ref, _ = O.static_act_scale(ax, si_ref)
+    xq_ref, xs_ref, clip_ref = O.quant_act_static(c.x_f32(), si_ref, d_ref)
+    wq_ref, ws_ref, _ = O.fold_quantize_weight(c.w_f32(), s_ref)
+    rows = sample_rows(c)
+    acc_ref, y_ref = O.w8a8_gemm(xq_ref, xs_ref, wq_ref, ws_ref, rows=rows)
+    layer = pipeline.Layer.for_case(c, act_scale="static")
+    layer.load(dev(c.x, c.dtype), dev(c.w, c.dtype))
+    layer.step(want_acc=True)
+    torch.cuda.synchronize()
+    assert int(layer.flags.item()) == 0
+    assert f32bits(layer.d)[0] == npbits([d_ref])[0]
+    assert int(layer.clipped.item()) == clip_ref == 0   # calibrated on the same X
+    assert np.array_equal(codes_np(layer.xq), xq_ref)
+    assert np.array_equal(f32bits(layer.x_scale), npbits(xs_ref))
+    rows_t = torch.from_numpy(rows).cuda()
+    assert np.array_equal(layer.acc.index_select(0, rows_t).cpu().numpy().astype(np.int64), acc_ref)
+    assert O.bf16_ulp_distance(y_bits(layer.y.index_select(0, rows_t)), y_ref).max() <= 1
+
+
+# ------------------------------------------------------------------ diagnostics
+def _rel_close(got, want, rel, floor=0.0):
+    got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    return np.all(np.abs(got - want) <= rel * np.abs(want) + floor)
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+@pytest.mark.parametrize("p", SMALL, ids=[p["name"] for p in SMALL])
+def test_diagnostics_match_oracle(sq, p, codes):
+    c = make_small(p)
+    if (c.cin * (2 if c.dtype == "bf16" else 4)) % 16:
+        pytest.skip("activation rows must be 16-byte aligned")
+    xf, wf = c.x_f32(), c.w_f32()
+    r = O.run_path(xf, wf, c.alpha)
+    x_t, w_t = dev(c.x, c.dtype), dev(c.w, c.dtype)
+    si, s = torch.from_numpy(r["s_inv"]).cuda(), torch.from_numpy(r["s"]).cuda()
+    cdt = torch.bfloat16 if codes == "bf16" else torch.int8
+    xq = torch.from_numpy(r["xq"].astype(F32 if codes == "bf16" else np.int8)).to(cdt).cuda()
+    wq = torch.from_numpy(r["wq"].astype(F32 if codes == "bf16" else np.int8)).to(cdt).cuda()
+    xs, ws = torch.from_numpy(r["x_scale"]).cuda(), torch.from_numpy(r["w_scale"]).cuda()
+    ea = sq.act_quant_error(x_t, si, xq, xs).cpu().numpy()
+    assert _rel_close(ea, O.act_quant_error(xf, r["s_inv"], r["xq"], r["x_scale"]), 1e-12)
+    ew = sq.weight_quant_error(w_t, s, wq, ws).cpu().numpy()
+    assert _rel_close(ew, O.weight_quant_error(wf, r["s"], r["wq"], r["w_scale"]), 1e-12)
+    y = torch.from_numpy(r["y"].view(np.int16)).view(torch.bfloat16).cuda()
+    rows = np.arange(0, c.tokens, max(1, c.tokens // 7))[:64]
+    el = sq.layer_error(x_t, w_t, y, torch.from_numpy(rows.astype(np.int32))).cpu().numpy()
+    ref = O.layer_error(xf, wf, r["y"], rows)
+    assert _rel_close(el, ref, 1e-4, floor=1e-12)
+    ax = torch.from_numpy(r["amax_x"]).cuda()
+    for scale in (None, si):
+        got = sq.channel_stats(ax, scale).cpu().numpy()
+        want = O.channel_stats(r["amax_x"], None if scale is None else r["s_inv"])
+        assert _rel_close(got, want, 1e-12)
+
+
+def test_alpha_sweep_matches_oracle(sq):
+    from w8a8_post_quantization_02_b300 import pipeline
+    c = synth.workload("single_linear_64x512x512")
+    rows = np.arange(0, 64, 3)
+    res = pipeline.alpha_sweep(dev(c.x, c.dtype), dev(c.w, c.dtype), [0.3, 0.5, 0.7, 0.9], codes="bf16",
+                               rows=torch.from_numpy(rows.astype(np.int32)))
+    xf, wf = c.x_f32(), c.w_f32()
+    for got in res:
+        r = O.run_path(xf, wf, got["alpha"])
+        assert _rel_close(got["act_error"], O.act_quant_error(xf, r["s_inv"], r["xq"], r["x_scale"]).sum(), 1e-12)
+        assert _rel_close(got["weight_error"], O.weight_quant_error(wf, r["s"], r["wq"], r["w_scale"]).sum(), 1e-12)
+        assert _rel_close(got["layer_error"], O.layer_error(xf, wf, r["y"], rows).sum(), 1e-4)
+        assert _rel_close(got["x_difficulty_smoothed"], O.channel_stats(r["amax_x"], r["s_inv"])[1], 1e-12)
+        assert _rel_close(got["w_difficulty_smoothed"], O.channel_stats(r["amax_w"], r["s"])[1], 1e-12)
+    # smoothing moves the spread from X to W as alpha grows (pages: migrate
+    # quantization difficulty from activations into weights)
+    xd = [g["x_difficulty_smoothed"] for g in res]
+    wd = [g["w_difficulty_smoothed"] for g in res]
+    assert xd == sorted(xd, reverse=True) and wd == sorted(wd)
+
+
+def test_full_workload_diagnostics(sq):
+    from w8a8_post_quantization_02_b300 import pipeline
+    c = synth.workload("down_proj_2048x11008x4096")
+    layer = pipeline.Layer.for_case(c)
+    layer.load(dev(c.x, c.dtype), dev(c.w, c.dtype))
+    layer.step()
+    rows = sample_rows(c)[:64]
+    d = pipeline.diagnose(layer, torch.from_numpy(rows.astype(np.int32)))
+    xf, wf = c.x_f32(), c.w_f32()
+    ax, aw = O.calibrate_absmax(xf, 0), O.calibrate_absmax(wf, 1)
+    s_ref, si_ref, _ = O.smooth_factors(ax, aw, c.alpha)
+    wq_ref, ws_ref, _ = O.fold_quantize_weight(wf, s_ref)
+    xq_ref, xs_ref, _ = O.quant_act(xf, si_ref)
+    assert _rel_close(d["act_error"], O.act_quant_error(xf, si_ref, xq_ref, xs_ref).sum(), 1e-11)
+    assert _rel_close(d["weight_error"], O.weight_quant_error(wf, s_ref, wq_ref, ws_ref).sum(), 1e-11)
+    # the layer error of the GPU's own output (within 1 bf16 ulp of the oracle's)
+    assert _rel_close(d["layer_error"], O.layer_error(xf, wf, y_bits(layer.y), rows).sum(), 1e-4)
+    assert _rel_close(d["x_difficulty"], O.channel_stats(ax)[1], 1e-12)

@@ -368,3 +368,105 @@ def test_ulp_distance_helper():
     a = np.array([0x3F80, 0x3F80, 0x8001, 0x0000], np.uint16)
     b = np.array([0x3F81, 0x3F80, 0x0001, 0x8000], np.uint16)
     assert O.bf16_ulp_distance(a, b).tolist() == [1, 0, 2, 0]
+
+
+
+# ---------------------------------------------------------------- static activation scale
+def test_static_scale_is_the_tensor_maximum():
+    """d from the per-channel maxima equals max|X'| / 127 over every element
+    (brute force over the tensor), for mixed signs and outlier channels."""
+    c = synth.make_case("st", 97, 160, 8, dtype="bf16", outlier_frac=0.05, seed=3)
+    x = c.x_f32()
+    si = (0.1 + 3.0 * synth.uniform(5, 50, 160)).astype(F32)
+    d, nf = O.static_act_scale(O.calibrate_absmax(x, 0), si)
+    brute = max(abs(float(F32(F32(v) * F32(s)))) for row in x for v, s in zip(row, si))
+    assert not nf and d == F32(F32(brute) / F32(127))
+
+
+def test_static_codes_reduce_to_dynamic_for_one_token():
+    """With one token calibrated on itself the static scale is that token's
+    dynamic scale, so the codes are identical."""
+    c = synth.make_case("st1", 1, 256, 8, dtype="bf16", outlier_frac=0.02, seed=4)
+    x = c.x_f32()
+    si = (0.5 + synth.uniform(6, 51, 256)).astype(F32)
+    d, _ = O.static_act_scale(O.calibrate_absmax(x, 0), si)
+    qs, xs_s, clipped = O.quant_act_static(x, si, d)
+    qd, xs_d, _ = O.quant_act(x, si)
+    assert clipped == 0 and np.array_equal(qs, qd) and xs_s[0] == xs_d[0]
+
+
+def test_static_codes_clip_beyond_calibration():
+    """Runtime values past the calibrated maximum saturate at +-127 and are
+    counted; a value at exactly 127.5 steps rounds to 128 (half to even)
+    and is clipped, 127.25 steps is not."""
+    d = F32(1.0)
+    si = np.ones(6, F32)
+    x = np.array([[127.25, 127.5, -300.0, 254.0, 0.5, -1.5]], F32)
+    q, xs, clipped = O.quant_act_static(x, si, d)
+    assert q[0].tolist() == [127, 127, -127, 127, 0, -2]
+    assert clipped == 3 and xs[0] == F32(1.0)
+
+
+
+# ---------------------------------------------------------------- diagnostics
+def test_quant_errors_match_exact_rationals():
+    """Activation and weight reconstruction errors against the definition in
+    exact rational arithmetic on a tiny layer."""
+    x = synth.normal(7, 1, 3 * 8, 1.0).reshape(3, 8).astype(F32)
+    w = synth.normal(7, 2, 8 * 5, 0.02).reshape(8, 5).astype(F32)
+    r = O.run_path(x, w, 0.5)
+    ea = O.act_quant_error(x, r["s_inv"], r["xq"], r["x_scale"])
+    ew = O.weight_quant_error(w, r["s"], r["wq"], r["w_scale"])
+    for t in range(3):
+        exact = sum((Fr(float(F32(x[t, j] * r["s_inv"][j]))) - int(r["xq"][t, j]) * Fr(float(r["x_scale"][t]))) ** 2
+                    for j in range(8))
+        assert abs(Fr(float(ea[t])) - exact) <= exact * Fr(1, 10 ** 12)
+    for n in range(5):
+        exact = sum((Fr(float(F32(r["s"][j] * w[j, n]))) - int(r["wq"][n, j]) * Fr(float(r["w_scale"][n]))) ** 2
+                    for j in range(8))
+        assert abs(Fr(float(ew[n])) - exact) <= exact * Fr(1, 10 ** 12)
+
+
+def test_quant_error_bounds():
+    """Round to nearest: every element is off by at most half a step, so the
+    error of a row is at most K * (d / 2)^2, and a row that is already a
+    multiple of its step has error 0."""
+    c = synth.make_case("eb", 40, 96, 24, dtype="bf16", outlier_frac=0.05, seed=9)
+    r = O.run_path(c.x_f32(), c.w_f32(), 0.5)
+    ea = O.act_quant_error(c.x_f32(), r["s_inv"], r["xq"], r["x_scale"])
+    assert (ea <= 96 * (r["x_scale"].astype(np.float64) / 2) ** 2).all() and (ea > 0).all()
+    ew = O.weight_quant_error(c.w_f32(), r["s"], r["wq"], r["w_scale"])
+    assert (ew <= 96 * (r["w_scale"].astype(np.float64) / 2) ** 2).all()
+    grid = np.arange(-127, 128, dtype=F32)[None, :]      # max 127: step exactly 1
+    q, d, _ = O.quant_act(grid, np.ones(255, F32))
+    assert d[0] == 1.0 and O.act_quant_error(grid, np.ones(255, F32), q, d)[0] == 0.0
+
+
+def test_layer_error_definition():
+    """The layer error of the exact product rounded to bf16 is the rounding
+    alone (tiny, bounded by half a bf16 ulp per element), and the error of
+    a quantized layer matches a float64 loop."""
+    x = synth.normal(8, 1, 4 * 16, 1.0).reshape(4, 16).astype(F32)
+    w = synth.normal(8, 2, 16 * 6, 0.1).reshape(16, 6).astype(F32)
+    exact = x.astype(np.float64) @ w.astype(np.float64)
+    e0 = O.layer_error(x, w, O.bf16_rne_bits(exact), np.arange(4))
+    assert (e0 <= 6 * (np.abs(exact).max(axis=1) * 2.0 ** -8) ** 2).all()
+    r = O.run_path(x, w, 0.5)
+    e = O.layer_error(x, w, r["y"], [1, 3])
+    yf = (r["y"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    loop = [sum((sum(float(x[t, j]) * float(w[j, n]) for j in range(16)) - yf[t, n]) ** 2 for n in range(6))
+            for t in (1, 3)]
+    assert np.allclose(e, loop, rtol=1e-12, atol=0)
+
+
+def test_channel_stats_against_statistics_module():
+    import statistics
+    amax = np.abs(synth.normal(9, 3, 300, 1.0)).astype(F32)
+    amax[[5, 77]] *= F32(60.0)
+    scale = (0.5 + synth.uniform(9, 4, 300)).astype(F32)
+    m, sd = O.channel_stats(amax)
+    assert m == pytest.approx(statistics.fmean(amax.astype(float)), rel=1e-13)
+    assert sd == pytest.approx(statistics.pstdev(amax.astype(float)), rel=1e-12)
+    m2, sd2 = O.channel_stats(amax, scale)
+    v = [float(F32(a * b)) for a, b in zip(amax, scale)]
+    assert sd2 == pytest.approx(statistics.pstdev(v), rel=1e-12)

@@ -15,7 +15,9 @@
 // the row's max|X'|; one block barrier combines the warps' maxima (and
 // frees the stage for the next copy); pass 2 writes the codes.  HBM
 // traffic per element: one read of X and one write of the code, plus 4
-// bytes per token for the scale.
+// bytes per token for the scale.  The same kernel serves the static
+// variant (one calibrated scale for every token, SmoothQuant glossary:
+// calibration-based): no row maximum, the clamp can act and is counted.
 #include "sq_async.cuh"
 
 namespace sq {
@@ -61,13 +63,16 @@ SQ_DEVINL void load_sinv(const float* s_inv, int64_t e0, float* f) {
 // v = tid + i*NT).  With NT <= 512 the thread's s^-1 values stay in
 // registers; with 1024 threads (rows longer than 32 KiB) the register
 // budget is 64 per thread, so they are re-read through L1 for each row.
-template <bool BF16, int CODES, int NT, int VPT>
+// STATIC: one calibrated scale *d_static for every token instead of the
+// row maximum (no reduction; the clamp can act and `clipped` counts it).
+template <bool BF16, int CODES, int NT, int VPT, bool STATIC>
 __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x, int64_t tokens,
                                                   int nvec, int64_t ldx_bytes,
                                                   const float* __restrict__ s_inv,
                                                   uint8_t* __restrict__ xq,
                                                   float* __restrict__ x_scale, int32_t* flags,
-                                                  int stages) {
+                                                  int stages, const float* __restrict__ d_static,
+                                                  uint32_t* clipped) {
   constexpr int E = BF16 ? 8 : 4;
   constexpr int NW = NT / 32;
   constexpr int CB = CODES == SQ_CODES_BF16 ? 2 : 1;
@@ -107,6 +112,13 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
     }
   }
 
+  float d_fix = 1.0f, inv_fix = 1.0f;
+  if constexpr (STATIC) {
+    d_fix = *d_static;
+    inv_fix = __fdiv_rn(1.0f, d_fix);
+  }
+  uint32_t nclip = 0u;
+  bool nonfinite = false;
   int it = 0;
   bool aborted = false;
   for (int64_t r = blockIdx.x; r < tokens; r += gridDim.x, ++it) {
@@ -132,15 +144,19 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
         }
 #pragma unroll
         for (int e = 0; e < E; e += 2) mul2_rn(p[i][e], p[i][e + 1], sv[e], sv[e + 1]);
+        if constexpr (!STATIC) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) m = absmax_nan(m, p[i][e]);
+          for (int e = 0; e < E; ++e) m = absmax_nan(m, p[i][e]);
+        }
       } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) p[i][e] = 0.0f;
       }
     }
-    uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
-    if (lane == 0) red[(it & 1) * NW + warp] = mb;
+    if constexpr (!STATIC) {
+      const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
+      if (lane == 0) red[(it & 1) * NW + warp] = mb;
+    }
     if (__syncthreads_or(!ok)) {
       aborted = true;
       break;
@@ -154,19 +170,27 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
         bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
       }
     }
-    uint32_t amax = 0u;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) amax = max(amax, red[(it & 1) * NW + w]);
     float d, inv;
-    scale_and_inverse(__uint_as_float(amax), d, inv);
-    if (tid == 0) {
-      x_scale[r] = d;
-      if (!finite_bits(amax)) raise_flag(flags, SQ_FLAG_NONFINITE);
+    bool no_clamp;
+    if constexpr (STATIC) {
+      d = d_fix;
+      inv = inv_fix;
+      no_clamp = false;
+      if (tid == 0) x_scale[r] = d;
+    } else {
+      uint32_t amax = 0u;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) amax = max(amax, red[(it & 1) * NW + w]);
+      scale_and_inverse(__uint_as_float(amax), d, inv);
+      if (tid == 0) {
+        x_scale[r] = d;
+        if (!finite_bits(amax)) raise_flag(flags, SQ_FLAG_NONFINITE);
+      }
+      // With a finite max >= 2^-119, d = RN(amax/127) and 1/d are normal, so
+      // |X' * (1/d)| <= 127 * (1 + 3 * 2^-24) < 127.5 and the clamp to
+      // [-127, 127] can never change a code: it is skipped.
+      no_clamp = amax >= 0x04000000u && amax < 0x7F800000u;
     }
-    // With a finite max >= 2^-119, d = RN(amax/127) and 1/d are normal, so
-    // |X' * (1/d)| <= 127 * (1 + 3 * 2^-24) < 127.5 and the clamp to
-    // [-127, 127] can never change a code: it is skipped.
-    const bool no_clamp = amax >= 0x04000000u && amax < 0x7F800000u;
 
     // pass 2: codes = rne(X' * (1/d)), via the magic-number add
     uint8_t* qrow = xq + r * (int64_t)nvec * E * CB;
@@ -181,6 +205,18 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
         // round ties of X'/d differently from rne(RN(X' * (1/d)))
 #pragma unroll
         for (int e = 0; e < E; ++e) q[e] = __fadd_rn(__fmul_rn(p[i][e], inv), kMagic);
+      } else if constexpr (STATIC) {
+        // scalar multiply, clamp, then the rounding add.  A NaN gives code 0
+        // and +-inf saturates; neither counts as clipped, both are flagged.
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float t = __fmul_rn(p[i][e], inv);
+          const float a = fabsf(t);
+          const bool finite = a <= 3.4028234663852886e38f;
+          nonfinite |= !finite;
+          nclip += (finite && a >= 127.5f) ? 1u : 0u;
+          q[e] = __fadd_rn((t == t) ? fminf(fmaxf(t, -127.0f), 127.0f) : 0.0f, kMagic);
+        }
       } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) q[e] = code_magic(p[i][e], inv);
@@ -207,6 +243,13 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
     }
   }
 
+  if constexpr (STATIC) {
+    if (clipped) {
+      nclip = __reduce_add_sync(0xFFFFFFFFu, nclip);
+      if (lane == 0 && nclip) atomicAdd(clipped, nclip);
+    }
+    if (__any_sync(0xFFFFFFFFu, nonfinite) && lane == 0) raise_flag(flags, SQ_FLAG_NONFINITE);
+  }
   if (aborted && tid == 0) {
     raise_flag(flags, SQ_FLAG_TIMEOUT);
     // let every copy this CTA issued land before its shared memory is freed
@@ -224,11 +267,16 @@ struct ActLaunch {
   int grid;
 };
 
-template <bool BF16, int CODES, int NT, int VPT>
+struct Static {
+  const float* d;      // null: per-token scales
+  uint32_t* clipped;
+};
+
+template <bool BF16, int CODES, int NT, int VPT, bool STATIC>
 sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
-                     const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
+                     const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags, Static sc,
                      cudaStream_t st) {
-  auto kern = k_quant_act<BF16, CODES, NT, VPT>;
+  auto kern = k_quant_act<BF16, CODES, NT, VPT, STATIC>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
@@ -246,35 +294,61 @@ sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_byt
   occ = std::max(1, std::min(occ, 4));
   const int64_t grid = std::min<int64_t>(tokens, (int64_t)sm_count() * occ);
   kern<<<(unsigned)grid, NT, smem, st>>>(x, tokens, nvec, ldx_bytes, s_inv, xq, x_scale, flags,
-                                         stages);
+                                         stages, sc.d, sc.clipped);
   return launch_status();
+}
+
+template <bool BF16, int CODES, int NT, bool STATIC>
+sq_status launch_act_vpt(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
+                         const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
+                         Static sc, cudaStream_t st) {
+  switch ((nvec + NT - 1) / NT) {
+    case 1: return launch_act<BF16, CODES, NT, 1, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case 2: return launch_act<BF16, CODES, NT, 2, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case 3: return launch_act<BF16, CODES, NT, 3, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case 4: return launch_act<BF16, CODES, NT, 4, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    default: return SQ_ERR_UNSUPPORTED;
+  }
 }
 
 template <bool BF16, int CODES, int NT>
 sq_status launch_act_nt(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
                         const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
-                        cudaStream_t st) {
-  switch ((nvec + NT - 1) / NT) {
-    case 1: return launch_act<BF16, CODES, NT, 1>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
-    case 2: return launch_act<BF16, CODES, NT, 2>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
-    case 3: return launch_act<BF16, CODES, NT, 3>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
-    case 4: return launch_act<BF16, CODES, NT, 4>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
-    default: return SQ_ERR_UNSUPPORTED;
-  }
+                        Static sc, cudaStream_t st) {
+  return sc.d ? launch_act_vpt<BF16, CODES, NT, true>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st)
+              : launch_act_vpt<BF16, CODES, NT, false>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
 }
 
 template <bool BF16, int CODES>
 sq_status launch_act_codes(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
                            const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
-                           cudaStream_t st) {
+                           Static sc, cudaStream_t st) {
   // the smallest block whose threads hold the row in at most 4 vectors each
   if (nvec <= 128 * 4)
-    return launch_act_nt<BF16, CODES, 128>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+    return launch_act_nt<BF16, CODES, 128>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
   if (nvec <= 256 * 4)
-    return launch_act_nt<BF16, CODES, 256>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+    return launch_act_nt<BF16, CODES, 256>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
   if (nvec <= 512 * 4)
-    return launch_act_nt<BF16, CODES, 512>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
-  return launch_act_nt<BF16, CODES, 1024>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, st);
+    return launch_act_nt<BF16, CODES, 512>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+  return launch_act_nt<BF16, CODES, 1024>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+}
+
+sq_status quant_act_any(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                        const float* s_inv, void* xq, sq_codes fmt, float* x_scale,
+                        int32_t* flags, Static sc, cudaStream_t st) {
+  const bool bf16 = dt == SQ_BF16;
+  const int nvec = (int)(cin / (bf16 ? 8 : 4));
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  uint8_t* qb = static_cast<uint8_t*>(xq);
+  const int64_t ldb = ldx * elem_bytes(dt);
+  if (bf16) {
+    return fmt == SQ_CODES_BF16
+               ? launch_act_codes<true, SQ_CODES_BF16>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, sc, st)
+               : launch_act_codes<true, SQ_CODES_I8>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, sc, st);
+  }
+  return fmt == SQ_CODES_BF16
+             ? launch_act_codes<false, SQ_CODES_BF16>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, sc, st)
+             : launch_act_codes<false, SQ_CODES_I8>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, sc, st);
 }
 
 }  // namespace
@@ -286,19 +360,13 @@ int64_t quant_act_max_cin(sq_dtype dt) { return (int64_t)4096 * (dt == SQ_BF16 ?
 sq_status quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
                     const float* s_inv, void* xq, sq_codes fmt, float* x_scale, int32_t* flags,
                     cudaStream_t st) {
-  const bool bf16 = dt == SQ_BF16;
-  const int nvec = (int)(cin / (bf16 ? 8 : 4));
-  const uint8_t* xb = static_cast<const uint8_t*>(x);
-  uint8_t* qb = static_cast<uint8_t*>(xq);
-  const int64_t ldb = ldx * elem_bytes(dt);
-  if (bf16) {
-    return fmt == SQ_CODES_BF16
-               ? launch_act_codes<true, SQ_CODES_BF16>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st)
-               : launch_act_codes<true, SQ_CODES_I8>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st);
-  }
-  return fmt == SQ_CODES_BF16
-             ? launch_act_codes<false, SQ_CODES_BF16>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st)
-             : launch_act_codes<false, SQ_CODES_I8>(nvec, xb, tokens, ldb, s_inv, qb, x_scale, flags, st);
+  return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags, Static{nullptr, nullptr}, st);
+}
+
+sq_status quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                           const float* s_inv, const float* d, void* xq, sq_codes fmt,
+                           float* x_scale, uint32_t* clipped, int32_t* flags, cudaStream_t st) {
+  return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags, Static{d, clipped}, st);
 }
 
 }  // namespace sq

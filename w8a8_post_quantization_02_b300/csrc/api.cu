@@ -11,7 +11,18 @@ sq_status fold_quantize_weight(const void*, sq_dtype, int64_t, int64_t, int64_t,
 sq_status quant_act(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, void*,
                     sq_codes, float*, int32_t*, cudaStream_t);
 int64_t quant_act_max_cin(sq_dtype);
+sq_status static_act_scale(const float*, const float*, int64_t, float*, int32_t*, cudaStream_t);
+sq_status quant_act_static(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*,
+                           const float*, void*, sq_codes, float*, uint32_t*, int32_t*, cudaStream_t);
 int fold_kernel_count(sq_dtype, int64_t, int64_t, int64_t);
+sq_status act_quant_error(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, const void*,
+                          sq_codes, const float*, double*, cudaStream_t);
+sq_status weight_quant_error(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*,
+                             const void*, sq_codes, const float*, double*, cudaStream_t);
+int layer_error_max_rows();
+sq_status layer_error(const void*, const void*, sq_dtype, int64_t, int64_t, int64_t, int64_t,
+                      const void*, const int32_t*, int, double*, cudaStream_t);
+sq_status channel_stats(const float*, const float*, int64_t, double*, cudaStream_t);
 int calibrate_kernel_count(sq_dtype, int64_t, int64_t, int64_t, int, int);
 sq_status gemm_i8_mma(const int8_t*, const float*, const int8_t*, const float*, int64_t, int64_t,
                       int64_t, void*, int32_t*, cudaStream_t);
@@ -66,6 +77,8 @@ int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int6
     case SQ_OP_SMOOTH: return 1;
     case SQ_OP_FOLD_QUANTIZE: return fold_kernel_count(dt, k, n, ld);
     case SQ_OP_QUANT_ACT: return 1;
+    case SQ_OP_STATIC_SCALE: return 1;
+    case SQ_OP_QUANT_ACT_STATIC: return 1;
     case SQ_OP_GEMM: return 1;
   }
   return -1;
@@ -115,6 +128,70 @@ sq_status sq_quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, 
     return SQ_ERR_INVALID_ARG;
   if (cin > quant_act_max_cin(dt)) return SQ_ERR_UNSUPPORTED;
   return quant_act(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, dev_flags, stream);
+}
+
+sq_status sq_static_act_scale(const float* amax_x, const float* s_inv, int64_t cin, float* d,
+                              int32_t* dev_flags, cudaStream_t stream) {
+  if (!amax_x || !s_inv || !d || cin < 1) return SQ_ERR_INVALID_ARG;
+  return static_act_scale(amax_x, s_inv, cin, d, dev_flags, stream);
+}
+
+sq_status sq_quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                              const float* s_inv, const float* d, void* xq, sq_codes fmt,
+                              float* x_scale, uint32_t* clipped, int32_t* dev_flags,
+                              cudaStream_t stream) {
+  if (!x || !s_inv || !d || !xq || !x_scale || !valid_dtype(dt) || !valid_codes(fmt) ||
+      tokens < 1 || cin < 1 || ldx < cin || cin % 16 != 0)
+    return SQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || (ldx * elem_bytes(dt)) % 16 != 0 || !aligned16(xq) || !aligned16(s_inv) ||
+      (reinterpret_cast<uintptr_t>(clipped) & 3))
+    return SQ_ERR_INVALID_ARG;
+  if (cin > ((int64_t)1 << 30)) return SQ_ERR_UNSUPPORTED;
+  return quant_act_static(x, dt, tokens, cin, ldx, s_inv, d, xq, fmt, x_scale, clipped, dev_flags,
+                          stream);
+}
+
+sq_status sq_act_quant_error(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                             const float* s_inv, const void* xq, sq_codes fmt, const float* x_scale,
+                             double* err, cudaStream_t stream) {
+  if (!x || !s_inv || !xq || !x_scale || !err || !valid_dtype(dt) || !valid_codes(fmt) || tokens < 1 ||
+      cin < 1 || ldx < cin || cin % 16 != 0)
+    return SQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || (ldx * elem_bytes(dt)) % 16 != 0 || !aligned16(xq) ||
+      (reinterpret_cast<uintptr_t>(err) & 7))
+    return SQ_ERR_INVALID_ARG;
+  return act_quant_error(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, err, stream);
+}
+
+sq_status sq_weight_quant_error(const void* w, sq_dtype dt, int64_t cin, int64_t cout, int64_t ldw,
+                                const float* s, const void* wq, sq_codes fmt, const float* w_scale,
+                                double* err, cudaStream_t stream) {
+  if (!w || !s || !wq || !w_scale || !err || !valid_dtype(dt) || !valid_codes(fmt) || cin < 1 ||
+      cout < 1 || ldw < cout)
+    return SQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w) % elem_bytes(dt)) != 0 || (reinterpret_cast<uintptr_t>(err) & 7))
+    return SQ_ERR_INVALID_ARG;
+  return weight_quant_error(w, dt, cin, cout, ldw, s, wq, fmt, w_scale, err, stream);
+}
+
+sq_status sq_layer_error(const void* x, const void* w, sq_dtype dt, int64_t tokens, int64_t cin,
+                         int64_t cout, int64_t ldx, int64_t ldw, const void* y,
+                         const int32_t* rows, int nrows, double* err, cudaStream_t stream) {
+  (void)tokens;
+  if (!x || !w || !y || !rows || !err || !valid_dtype(dt) || tokens < 1 || cin < 1 || cout < 1 ||
+      ldx < cin || ldw < cout || nrows < 1 || nrows > layer_error_max_rows())
+    return SQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) % elem_bytes(dt)) != 0 ||
+      (reinterpret_cast<uintptr_t>(w) % elem_bytes(dt)) != 0 || (reinterpret_cast<uintptr_t>(y) & 1) ||
+      (reinterpret_cast<uintptr_t>(rows) & 3) || (reinterpret_cast<uintptr_t>(err) & 7))
+    return SQ_ERR_INVALID_ARG;
+  return layer_error(x, w, dt, cin, cout, ldx, ldw, y, rows, nrows, err, stream);
+}
+
+sq_status sq_channel_stats(const float* amax, const float* scale, int64_t n, double* out,
+                           cudaStream_t stream) {
+  if (!amax || !out || n < 1 || (reinterpret_cast<uintptr_t>(out) & 7)) return SQ_ERR_INVALID_ARG;
+  return channel_stats(amax, scale, n, out, stream);
 }
 
 sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq, const float* w_scale,

@@ -7,10 +7,11 @@
 // weights).  This path reads the int8 weight codes directly, one byte per
 // weight, so it is the weight-streaming (decode, small m) path.
 //
-// A block owns 16*MT tokens x 16 output channels and its 8 warps split K.
-// Each lane loads 16 contiguous codes per row per 64-wide k step; the same
-// permutation of k inside the step is used for A and B, so every product
-// pairs matching k and the sum is unchanged.
+// A block owns 16*MT tokens x 16 output channels and its 8 warps split K
+// in runs of 8/MT consecutive 64-wide steps whose loads are all issued
+// before their MMAs.  Each lane loads 16 contiguous codes per row per step;
+// the same permutation of k inside the step is used for A and B, so every
+// product pairs matching k and the sum is unchanged.
 #include <cuda_bf16.h>
 
 #include "sq_common.cuh"
@@ -71,26 +72,37 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemm_i8_mma(
       arow[mt][h] = xq + (aval[mt][h] ? m : 0) * K;
     }
 
-  for (int64_t s = warp; s < nsteps; s += kWarps) {
-    const int64_t k = s * 64 + tq * 16;
-    const bool kin = k < K;
-    uint4 b[2];
+  // each warp takes U consecutive 64-wide k steps at a time and issues all
+  // of their loads before the MMAs, so U x 2 weight loads per lane are in
+  // flight (a decode step is bound by streaming the weights)
+  constexpr int U = 8 / MT;
+  for (int64_t s0 = (int64_t)warp * U; s0 < nsteps; s0 += (int64_t)kWarps * U) {
+    uint4 b[U][2];
+    uint4 a[U][MT][2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-      b[nt] = (kin && bval[nt]) ? ld_stream16(brow[nt] + k) : make_uint4(0u, 0u, 0u, 0u);
-    uint4 a[MT][2];
+    for (int u = 0; u < U; ++u) {
+      const int64_t k = (s0 + u) * 64 + tq * 16;
+      const bool kin = k < K;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+      for (int nt = 0; nt < 2; ++nt)
+        b[u][nt] = (kin && bval[nt]) ? ld_stream16(brow[nt] + k) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        a[mt][h] = (kin && aval[mt][h]) ? ld_ro16(arow[mt][h] + k) : make_uint4(0u, 0u, 0u, 0u);
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+        for (int h = 0; h < 2; ++h)
+          a[u][mt][h] = (kin && aval[mt][h]) ? ld_ro16(arow[mt][h] + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        mma_s8(acc[mt][nt], a[mt][0].x, a[mt][1].x, a[mt][0].y, a[mt][1].y, b[nt].x, b[nt].y);
-        mma_s8(acc[mt][nt], a[mt][0].z, a[mt][1].z, a[mt][0].w, a[mt][1].w, b[nt].z, b[nt].w);
-      }
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          mma_s8(acc[mt][nt], a[u][mt][0].x, a[u][mt][1].x, a[u][mt][0].y, a[u][mt][1].y, b[u][nt].x,
+                 b[u][nt].y);
+          mma_s8(acc[mt][nt], a[u][mt][0].z, a[u][mt][1].z, a[u][mt][0].w, a[u][mt][1].w, b[u][nt].z,
+                 b[u][nt].w);
+        }
   }
   __syncthreads();  // tile zeroed
 #pragma unroll

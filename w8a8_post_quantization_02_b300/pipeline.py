@@ -25,10 +25,13 @@ def choose_codes(tokens: int) -> str:
 
 class Layer:
     def __init__(self, tokens: int, cin: int, cout: int, dtype: str, alpha: float,
-                 codes: str | None = None, device="cuda"):
+                 codes: str | None = None, device="cuda", act_scale: str = "dynamic"):
+        if act_scale not in ("dynamic", "static"):
+            raise ValueError("act_scale is 'dynamic' (per token) or 'static' (one calibrated scale)")
         self.tokens, self.cin, self.cout = tokens, cin, cout
         self.dtype = dtype
         self.alpha = float(alpha)
+        self.act_scale = act_scale
         self.codes = codes or choose_codes(tokens)
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
         cdt = torch.bfloat16 if self.codes == "bf16" else torch.int8
@@ -46,6 +49,8 @@ class Layer:
         self.y = torch.empty(tokens, cout, dtype=torch.bfloat16, device=dv)
         self.acc = torch.empty(tokens, cout, dtype=torch.int32, device=dv)
         self.flags = torch.zeros(1, dtype=torch.int32, device=dv)
+        self.d = torch.empty(1, dtype=torch.float32, device=dv)          # static scale
+        self.clipped = torch.zeros(1, dtype=torch.int32, device=dv)      # static clip count
         fmt = sq._codes_fmt(self.codes)
         self._fmt = fmt
         ws_fold = sq.workspace_bytes(sq.SQ_OP_FOLD_QUANTIZE, 0, cout, cin, self.codes)
@@ -55,8 +60,9 @@ class Layer:
         self._lib = sq.load_library()
 
     @classmethod
-    def for_case(cls, case, codes: str | None = None) -> "Layer":
-        return cls(case.tokens, case.cin, case.cout, case.dtype, case.alpha, codes)
+    def for_case(cls, case, codes: str | None = None, act_scale: str = "dynamic") -> "Layer":
+        return cls(case.tokens, case.cin, case.cout, case.dtype, case.alpha, codes,
+                   act_scale=act_scale)
 
     def load(self, x: torch.Tensor, w: torch.Tensor) -> None:
         self.x.copy_(x)
@@ -74,6 +80,8 @@ class Layer:
             "smooth": K * 4 * 4,
             "fold_quantize": K * N * eb + N * K * cb + N * 4,
             "quant_act": T * K * eb + T * K * cb + T * 4 + K * 4,
+            "static_scale": K * 4 * 2 + 4,
+            "quant_act_static": T * K * eb + T * K * cb + T * 4 + K * 4,
             "gemm": (T + N) * K * cb + T * N * 2 + (T + N) * 4,
         }
 
@@ -116,8 +124,19 @@ class Layer:
                 ptr(self.y), ptr(self.acc) if want_acc else None, flags, ptr(self.ws_gemm),
                 self.ws_gemm.numel(), st))
 
-        fns = [("calibrate_x", calibrate_x), ("calibrate_w", calibrate_w), ("smooth", smooth),
-               ("fold_quantize", fold_quantize), ("quant_act", quant_act), ("gemm", gemm)]
+        def static_scale(st):
+            ck("sq_static_act_scale", L.sq_static_act_scale(ptr(self.amax_x), ptr(self.s_inv), K,
+                                                            ptr(self.d), flags, st))
+
+        def quant_act_static(st):
+            ck("sq_quant_act_static", L.sq_quant_act_static(
+                ptr(self.x), dt, T, K, K, ptr(self.s_inv), ptr(self.d), ptr(self.xq), self._fmt,
+                ptr(self.x_scale), ptr(self.clipped), flags, st))
+
+        act = ([("quant_act", quant_act)] if self.act_scale == "dynamic"
+               else [("static_scale", static_scale), ("quant_act_static", quant_act_static)])
+        fns = ([("calibrate_x", calibrate_x), ("calibrate_w", calibrate_w), ("smooth", smooth),
+                ("fold_quantize", fold_quantize)] + act + [("gemm", gemm)])
         return [(name, counts[name], fn) for name, fn in fns]
 
     def kernel_counts(self) -> dict:
@@ -130,12 +149,15 @@ class Layer:
             "smooth": sq.kernel_count(sq.SQ_OP_SMOOTH, dt, 0, 0, K),
             "fold_quantize": sq.kernel_count(sq.SQ_OP_FOLD_QUANTIZE, dt, 0, N, K, N),
             "quant_act": sq.kernel_count(sq.SQ_OP_QUANT_ACT, dt, T, 0, K, K),
+            "static_scale": sq.kernel_count(sq.SQ_OP_STATIC_SCALE, dt, 0, 0, K),
+            "quant_act_static": sq.kernel_count(sq.SQ_OP_QUANT_ACT_STATIC, dt, T, 0, K, K),
             "gemm": sq.kernel_count(sq.SQ_OP_GEMM, dt, T, N, K),
         }
 
     def kernel_count(self) -> int:
         """Library kernels one step enqueues."""
-        return sum(self.kernel_counts().values())
+        counts = self.kernel_counts()
+        return sum(counts[name] for name, _, _ in self.stages())
 
     def step(self, want_acc: bool = False, stream=None) -> None:
         st = sq._stream(stream)
@@ -164,3 +186,50 @@ class Layer:
 def available_codes():
     """Code formats whose GEMM path this build runs."""
     return ["i8", "bf16"]
+
+
+def diagnose(layer: "Layer", rows=None) -> dict:
+    """Quantization diagnostics of a layer after ``step()`` (float64 sums):
+    activation and weight reconstruction errors, the layer error on sampled
+    tokens (default: up to 64 evenly spaced), the channel-magnitude spread
+    ("quantization difficulty") of X before and after smoothing and of the
+    folded W, and the static-scale clip count when that mode ran."""
+    if rows is None:
+        n = min(64, layer.tokens)
+        rows = torch.linspace(0, layer.tokens - 1, n).round().to(torch.int32)
+    rows = torch.as_tensor(rows, dtype=torch.int32)
+    act = sq.act_quant_error(layer.x, layer.s_inv, layer.xq, layer.x_scale)
+    wgt = sq.weight_quant_error(layer.w, layer.s, layer.wq, layer.w_scale)
+    lay = sq.layer_error(layer.x, layer.w, layer.y, rows)
+    x_before = sq.channel_stats(layer.amax_x)
+    x_after = sq.channel_stats(layer.amax_x, layer.s_inv)
+    w_before = sq.channel_stats(layer.amax_w)
+    w_after = sq.channel_stats(layer.amax_w, layer.s)
+    out = {
+        "alpha": layer.alpha,
+        "act_error": float(act.sum()), "weight_error": float(wgt.sum()),
+        "layer_error": float(lay.sum()), "layer_error_rows": rows.numel(),
+        "x_difficulty": float(x_before[1]), "x_difficulty_smoothed": float(x_after[1]),
+        "w_difficulty": float(w_before[1]), "w_difficulty_smoothed": float(w_after[1]),
+    }
+    if layer.act_scale == "static":
+        out["clipped"] = int(layer.clipped.item())
+    return out
+
+
+def alpha_sweep(x: torch.Tensor, w: torch.Tensor, alphas, codes: str | None = None,
+                act_scale: str = "dynamic", rows=None) -> list:
+    """Run the whole path at each smoothing strength and return the
+    diagnostics of each (the pages select the strength on calibration or
+    development data; this gives the measurements to select by)."""
+    tokens, cin = x.shape
+    cout = w.shape[1]
+    dtype = "bf16" if x.dtype == torch.bfloat16 else "f32"
+    results = []
+    for a in alphas:
+        layer = Layer(tokens, cin, cout, dtype, float(a), codes, device=x.device, act_scale=act_scale)
+        layer.load(x, w)
+        layer.step()
+        results.append(diagnose(layer, rows))
+    torch.cuda.synchronize()
+    return results

@@ -19,7 +19,8 @@ SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_NONFINITE, SQ_ERR_CUDA, SQ_ERR_UNSUPPORTED, SQ
 SQ_FLAG_NONFINITE, SQ_FLAG_TIMEOUT = 1, 2
 SQ_F32, SQ_BF16 = 0, 1
 SQ_CODES_I8, SQ_CODES_BF16 = 0, 1
-SQ_OP_CALIBRATE, SQ_OP_SMOOTH, SQ_OP_FOLD_QUANTIZE, SQ_OP_QUANT_ACT, SQ_OP_GEMM = range(5)
+(SQ_OP_CALIBRATE, SQ_OP_SMOOTH, SQ_OP_FOLD_QUANTIZE, SQ_OP_QUANT_ACT, SQ_OP_GEMM, SQ_OP_STATIC_SCALE,
+ SQ_OP_QUANT_ACT_STATIC) = range(7)
 
 # name -> (restype, argtypes), mirroring include/sq.h
 _P, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -29,9 +30,15 @@ SIGNATURES = {
     "sq_fold_quantize_weight": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "sq_fold_quantize_weight_noalloc": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
+    "sq_static_act_scale": (_I32, [_P, _P, _I64, _P, _P, _P]),
+    "sq_quant_act_static": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _P, _P, _P]),
     "sq_w8a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "sq_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64, _I32]),
     "sq_kernel_count": (_I32, [_I32, _I32, _I64, _I64, _I64, _I64, _I32, _I32]),
+    "sq_act_quant_error": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
+    "sq_weight_quant_error": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
+    "sq_layer_error": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _I64, _I64, _P, _P, _I32, _P, _P]),
+    "sq_channel_stats": (_I32, [_P, _P, _I64, _P, _P]),
     "sq_status_string": (ctypes.c_char_p, [_I32]),
     "sq_check_device": (_I32, [_I32]),
 }
@@ -172,6 +179,34 @@ def quant_act(x: torch.Tensor, s_inv: torch.Tensor, codes: str = "i8",
     return xq, x_scale
 
 
+def static_act_scale(amax_x: torch.Tensor, s_inv: torch.Tensor, flags: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Step 4, static variant: the one calibrated scale d (a 1-element tensor)."""
+    d = out if out is not None else torch.empty(1, device=amax_x.device, dtype=torch.float32)
+    st = load_library().sq_static_act_scale(_ptr(amax_x), _ptr(s_inv), amax_x.numel(), _ptr(d),
+                                            _ptr(flags), _stream(stream))
+    _check("sq_static_act_scale", st)
+    return d
+
+
+def quant_act_static(x: torch.Tensor, s_inv: torch.Tensor, d: torch.Tensor, codes: str = "i8",
+                     clipped: torch.Tensor | None = None, flags: torch.Tensor | None = None,
+                     out=None, stream=None):
+    """Step 4 with the calibrated scale d: (xq codes, x_scale filled with d)."""
+    _check_cuda_2d(x, "x")
+    tokens, cin = x.shape
+    if out is None:
+        xq = torch.empty(tokens, cin, device=x.device, dtype=_codes_dtype(codes))
+        x_scale = torch.empty(tokens, device=x.device, dtype=torch.float32)
+    else:
+        xq, x_scale = out
+    st = load_library().sq_quant_act_static(_ptr(x), _dtype_code(x), tokens, cin, x.stride(0),
+                                            _ptr(s_inv), _ptr(d), _ptr(xq), _codes_fmt(codes),
+                                            _ptr(x_scale), _ptr(clipped), _ptr(flags), _stream(stream))
+    _check("sq_quant_act_static", st)
+    return xq, x_scale
+
+
 def w8a8_gemm(xq: torch.Tensor, x_scale: torch.Tensor, wq: torch.Tensor, w_scale: torch.Tensor,
               want_acc: bool = False, flags: torch.Tensor | None = None,
               workspace: torch.Tensor | None = None, out=None, stream=None):
@@ -194,6 +229,60 @@ def w8a8_gemm(xq: torch.Tensor, x_scale: torch.Tensor, wq: torch.Tensor, w_scale
         _stream(stream))
     _check("sq_w8a8_gemm", st)
     return (y, acc) if want_acc else y
+
+
+# ------------------------------------------------------------------ diagnostics
+def act_quant_error(x: torch.Tensor, s_inv: torch.Tensor, xq: torch.Tensor, x_scale: torch.Tensor,
+                    stream=None) -> torch.Tensor:
+    """Per-token squared reconstruction error of the activation codes (float64)."""
+    _check_cuda_2d(x, "x")
+    tokens, cin = x.shape
+    err = torch.empty(tokens, device=x.device, dtype=torch.float64)
+    codes = "bf16" if xq.dtype == torch.bfloat16 else "i8"
+    st = load_library().sq_act_quant_error(_ptr(x), _dtype_code(x), tokens, cin, x.stride(0), _ptr(s_inv),
+                                           _ptr(xq), _codes_fmt(codes), _ptr(x_scale), _ptr(err),
+                                           _stream(stream))
+    _check("sq_act_quant_error", st)
+    return err
+
+
+def weight_quant_error(w: torch.Tensor, s: torch.Tensor, wq: torch.Tensor, w_scale: torch.Tensor,
+                       stream=None) -> torch.Tensor:
+    """Per-output-channel squared reconstruction error of the folded weight (float64)."""
+    _check_cuda_2d(w, "w")
+    cin, cout = w.shape
+    err = torch.empty(cout, device=w.device, dtype=torch.float64)
+    codes = "bf16" if wq.dtype == torch.bfloat16 else "i8"
+    st = load_library().sq_weight_quant_error(_ptr(w), _dtype_code(w), cin, cout, w.stride(0), _ptr(s),
+                                              _ptr(wq), _codes_fmt(codes), _ptr(w_scale), _ptr(err),
+                                              _stream(stream))
+    _check("sq_weight_quant_error", st)
+    return err
+
+
+def layer_error(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, rows: torch.Tensor,
+                stream=None) -> torch.Tensor:
+    """Per sampled token: sum_n ((X W) - Y)^2 against the unquantized product (float64)."""
+    _check_cuda_2d(x, "x")
+    _check_cuda_2d(w, "w")
+    tokens, cin = x.shape
+    cout = w.shape[1]
+    rows = rows.to(device=x.device, dtype=torch.int32).contiguous()
+    err = torch.empty(rows.numel(), device=x.device, dtype=torch.float64)
+    st = load_library().sq_layer_error(_ptr(x), _ptr(w), _dtype_code(x), tokens, cin, cout, x.stride(0),
+                                       w.stride(0), _ptr(y.contiguous()), _ptr(rows), rows.numel(),
+                                       _ptr(err), _stream(stream))
+    _check("sq_layer_error", st)
+    return err
+
+
+def channel_stats(amax: torch.Tensor, scale: torch.Tensor | None = None, stream=None):
+    """(mean, population std) of the channel magnitudes (times scale if given), float64."""
+    out = torch.empty(2, device=amax.device, dtype=torch.float64)
+    st = load_library().sq_channel_stats(_ptr(amax), _ptr(scale), amax.numel(), _ptr(out),
+                                         _stream(stream))
+    _check("sq_channel_stats", st)
+    return out
 
 
 def smoothquant_linear(x: torch.Tensor, w: torch.Tensor, alpha: float, codes: str = "i8",
