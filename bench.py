@@ -48,8 +48,10 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--act-scale", choices=["dynamic", "static"], default="dynamic",
-                    help="per-token scales (default) or one calibrated scale per tensor")
+    ap.add_argument("--act-scale", choices=["dynamic", "static", "norm"], default="dynamic",
+                    help="per-token scales (default), one calibrated scale per tensor, or per-token "
+                         "scales after an RMS normalization whose gain absorbs S^-1 (the workload's X "
+                         "then stands for the normalization's input)")
     return ap.parse_args()
 
 
@@ -313,7 +315,8 @@ def run_ours(args, case_name):
         gbs = nbytes[name] / (us * 1e-6) / 1e9
         iso[name] = {"us": round(us, 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
     iso["gemm"]["tops"] = round(ops / (iso["gemm"]["us"] * 1e-6) / 1e12, 2)
-    act_stage = "quant_act" if args.act_scale == "dynamic" else "quant_act_static"
+    act_stage = {"dynamic": "quant_act", "static": "quant_act_static",
+                 "norm": "rmsnorm_quant_act"}[args.act_scale]
 
     bf16_peak = float(peaks["bf16_tflops"])
     if layer.codes == "bf16":

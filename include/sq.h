@@ -76,7 +76,9 @@ typedef enum {
   SQ_OP_QUANT_ACT = 3,
   SQ_OP_GEMM = 4,
   SQ_OP_STATIC_SCALE = 5,
-  SQ_OP_QUANT_ACT_STATIC = 6
+  SQ_OP_QUANT_ACT_STATIC = 6,
+  SQ_OP_FOLD_NORM_GAIN = 7,
+  SQ_OP_RMSNORM_QUANT_ACT = 8
 } sq_op;
 
 /*
@@ -217,6 +219,33 @@ sq_status sq_quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_
                               const float* s_inv, const float* d, void* xq, sq_codes fmt,
                               float* x_scale, uint32_t* clipped, int32_t* dev_flags,
                               cudaStream_t stream);
+
+/*
+ * Step 4 folded into the preceding RMS normalization.
+ * Source: first page, paragraph 3: to avoid an extra runtime scaling kernel
+ * the inverse factors may be folded into the preceding operation when every
+ * consumer keeps its compensation (one s for all consumers of the
+ * normalized activation, e.g. Q/K/V).  Reading: the preceding operation is
+ * an RMS normalization with a per-channel gain gamma (LLaMA-style layers).
+ *
+ * sq_fold_norm_gain (offline): gamma_folded[j] = RN(gamma[j] * s_inv[j]).
+ *   gamma, s_inv, gamma_folded  device fp32 [cin]
+ *
+ * sq_rmsnorm_quant_act (runtime, one kernel): for token t of the
+ * normalization's input h [tokens x cin],
+ *   S_t = the exact sum_j h[t,j]^2, rounded once to binary32
+ *   r_t = RN(1 / RN(sqrt(RN(RN(S_t / cin) + eps))))   (IEEE binary32 steps)
+ *   X'[t,j] = RN(RN(h[t,j] * r_t) * gamma_folded[j])
+ * followed by the dynamic per-token quantizer of sq_quant_act (same codes,
+ * x_scale, layouts, alignment and limits; h takes the place of x).  A
+ * non-finite row gives a non-finite scale and SQ_FLAG_NONFINITE.
+ */
+sq_status sq_fold_norm_gain(const float* gamma, const float* s_inv, int64_t cin,
+                            float* gamma_folded, cudaStream_t stream);
+sq_status sq_rmsnorm_quant_act(const void* h, sq_dtype dt, int64_t tokens, int64_t cin,
+                               int64_t ldh, const float* gamma_folded, float eps, void* xq,
+                               sq_codes fmt, float* x_scale, int32_t* dev_flags,
+                               cudaStream_t stream);
 
 /*
  * Step 5 - INT8 x INT8 GEMM with exact integer accumulation and a bf16

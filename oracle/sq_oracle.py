@@ -253,6 +253,90 @@ def quant_act_static(x, s_inv, d):
 
 
 # --------------------------------------------------------------------------
+# step 4 folded into the preceding normalization
+# --------------------------------------------------------------------------
+def fold_norm_gain(gamma, s_inv):
+    """gamma'_j = RN32(gamma_j * (1/s_j)).
+
+    First page, paragraph 3: instead of an extra runtime scaling kernel the
+    inverse factors may be folded into the preceding operation, provided
+    every consumer keeps its compensation (one s shared by all consumers of
+    the normalized activation).  Reading: the preceding operation is an RMS
+    normalization with a per-channel gain (LLaMA-style layers), whose gain
+    absorbs S^-1.
+    """
+    return (np.asarray(gamma, F32) * np.asarray(s_inv, F32)).astype(F32)
+
+
+def sum_squares_f32(row) -> np.float32:
+    """The exact sum of the squares of a binary32 row, rounded once to
+    binary32 (nearest, ties to even).
+
+    math.fsum gives the float64 rounding of the exact sum; rounding that
+    to binary32 equals rounding the exact sum directly unless the float64
+    value is itself a binary32 midpoint, in which case the exact sum (as an
+    integer multiple of 2^-300) decides.
+    """
+    import math
+    vals = np.asarray(row, F32)
+    s64 = math.fsum((vals.astype(np.float64) ** 2).tolist())   # squares exact in float64
+    f = F32(s64)
+    if float(f) == s64 or not np.isfinite(f):
+        return f
+    nb = np.nextafter(f, F32(np.inf) if s64 > float(f) else F32(0))
+    mid = (float(f) + float(nb)) / 2.0                        # exact: both binary32
+    if s64 != mid:
+        return f
+    # exact: h = m * 2^(e - 150), h^2 * 2^300 = m^2 * 2^(2e)
+    bits = vals.view(np.uint32) & np.uint32(0x7FFFFFFF)
+    total = 0
+    for b in bits.tolist():
+        e = b >> 23
+        m = (b & 0x7FFFFF) | (0x800000 if e else 0)
+        total += (m * m) << (2 * max(e, 1))
+    from fractions import Fraction
+    exact = Fraction(total, 2 ** 300)
+    mid_f = Fraction(mid)
+    if exact > mid_f:
+        return F32(max(float(f), float(nb)))
+    if exact < mid_f:
+        return F32(min(float(f), float(nb)))
+    return f if (int(np.asarray(f).view(np.uint32)) & 1) == 0 else nb
+
+
+def rms_inverse(h, eps):
+    """Per token r_t = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))) in binary32,
+    where S is the exact sum of squares rounded once to binary32
+    (``sum_squares_f32``) and every step is one IEEE binary32 operation."""
+    h32 = np.asarray(h, F32)
+    K = F32(h32.shape[1])
+    e32 = F32(eps)
+    out = np.empty(h32.shape[0], F32)
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore"):
+        for t in range(h32.shape[0]):
+            s = sum_squares_f32(h32[t])
+            ms = F32(F32(s / K) + e32)
+            out[t] = F32(F32(1.0) / np.sqrt(ms))
+    return out
+
+
+def rmsnorm_quant_act(h, gamma_folded, eps, return_scaled=False):
+    """X' = RN32(RN32(h * r_t) * gamma'_j), then the dynamic per-token
+    quantizer of step 4 (reading 4) on X'.  Returns ``(xq, x_scale,
+    nonfinite)`` (and X' with ``return_scaled``)."""
+    h32 = np.asarray(h, F32)
+    r = rms_inverse(h32, eps)
+    with np.errstate(over="ignore", invalid="ignore"):
+        xs = ((h32 * r[:, None]).astype(F32) * np.asarray(gamma_folded, F32)[None, :]).astype(F32)
+    amax = np.max(np.abs(xs), axis=1).astype(F32) if xs.shape[1] else np.zeros(xs.shape[0], F32)
+    d, inv, nonfinite = _scale_and_inverse(amax)
+    q = _codes(xs, inv[:, None])
+    if return_scaled:
+        return q, d, nonfinite, xs
+    return q, d, nonfinite
+
+
+# --------------------------------------------------------------------------
 # step 5: INT8 x INT8 -> exact accumulators -> bf16 epilogue
 # --------------------------------------------------------------------------
 def int_accumulate(xq, wq, rows=None) -> np.ndarray:
@@ -404,7 +488,8 @@ def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
 __all__ = [
     "calibrate_absmax", "rn32_pow", "smooth_factors", "fold_quantize_weight", "quant_act",
     "static_act_scale", "quant_act_static", "act_quant_error", "weight_quant_error",
-    "layer_error", "channel_stats",
+    "layer_error", "channel_stats", "fold_norm_gain", "sum_squares_f32", "rms_inverse",
+    "rmsnorm_quant_act",
     "int_accumulate", "bf16_rne_bits", "w8a8_gemm", "run_path", "bf16_ulp_distance",
     "STAT_FLOOR", "S_MIN", "S_MAX", "QMAX",
 ]

@@ -537,3 +537,48 @@ def test_full_workload_diagnostics(sq):
     # the layer error of the GPU's own output (within 1 bf16 ulp of the oracle's)
     assert _rel_close(d["layer_error"], O.layer_error(xf, wf, y_bits(layer.y), rows).sum(), 1e-4)
     assert _rel_close(d["x_difficulty"], O.channel_stats(ax)[1], 1e-12)
+
+
+# ------------------------------------------------------------------ RMSNorm fold
+NORM_SHAPES = [
+    (64, 512, "f32"), (37, 80, "bf16"), (300, 11008, "bf16"), (9, 16384, "f32"), (4099, 64, "bf16"),
+    (700, 4112, "bf16"), (40, 32768, "bf16"), (2048, 4096, "bf16"),
+]
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+@pytest.mark.parametrize("tokens,cin,dtype", NORM_SHAPES)
+def test_rmsnorm_fold_bit_exact(sq, tokens, cin, dtype, codes):
+    """Hidden states with outlier channels and a few massive tokens, a
+    random gain folded with random factors: codes and scales bit-exact."""
+    c = synth.make_case("nrm", tokens, cin, 16, dtype=dtype, outlier_frac=0.01, seed=tokens + 5 * cin,
+                        massive_tokens=min(3, tokens), massive_channels=2)
+    h = c.x.copy()
+    h[tokens // 2, :] = 0   # an all-zero token: r = 1/sqrt(eps)
+    if tokens > 2:
+        # a token whose float64 sum of squares is a binary32 midpoint that the
+        # exact sum lies above: 1 + 2^-24 + 2^-80 rounds up to 1 + 2^-23
+        crafted = np.zeros(cin, np.float64)
+        crafted[:3] = [1.0, 2.0 ** -12, 2.0 ** -40]
+        h[1] = synth.f64_to_bf16_bits(crafted) if dtype == "bf16" else crafted.astype(F32)
+    hf = synth.bf16_bits_to_f32(h) if dtype == "bf16" else h
+    gamma = (0.5 + synth.uniform(cin, 61, cin)).astype(F32)
+    si = (0.25 + 4.0 * synth.uniform(cin, 62, cin)).astype(F32)
+    eps = 1e-5
+    gf_ref = O.fold_norm_gain(gamma, si)
+    gf = sq.fold_norm_gain(torch.from_numpy(gamma).cuda(), torch.from_numpy(si).cuda())
+    assert np.array_equal(f32bits(gf), npbits(gf_ref))
+    q_ref, xs_ref, nf = O.rmsnorm_quant_act(hf, gf_ref, eps)
+    flags = flags_tensor()
+    xq, xs = sq.rmsnorm_quant_act(dev(h, dtype), gf, eps, codes, flags)
+    assert int(flags.item()) == 0 and not nf
+    assert np.array_equal(f32bits(xs), npbits(xs_ref))
+    assert np.array_equal(codes_np(xq), q_ref)
+
+
+def test_rmsnorm_nonfinite_flag(sq):
+    h = torch.ones(4, 64, device="cuda")
+    h[2, 9] = float("inf")
+    flags = flags_tensor()
+    sq.rmsnorm_quant_act(h, torch.ones(64, device="cuda"), 1e-6, "i8", flags)
+    assert int(flags.item()) & 1

@@ -39,6 +39,9 @@ def _pins():
         P.test_quant_error_bounds,
         P.test_layer_error_definition,
         P.test_channel_stats_against_statistics_module,
+        P.test_rms_inverse_against_high_precision,
+        P.test_sum_of_squares_rounds_the_exact_sum,
+        P.test_folded_gain_matches_unfolded_path,
     ]
     for seed in range(6):
         for kind, alpha in (("half", 0.5), ("one", 1.0), ("zero", 0.0)):
@@ -146,6 +149,20 @@ def stats_sample_std(amax, scale=None):
     return v.mean(), float(v.std(ddof=1))
 
 
+def rms_without_mean(h, eps):
+    h32 = np.asarray(h, F32).astype(np.float64)
+    return (1.0 / np.sqrt((h32 * h32).sum(axis=1) + float(F32(eps)))).astype(F32)   # sum, not mean
+
+
+def squares_rounded_through_float64(row):
+    import math
+    return F32(math.fsum((np.asarray(row, F32).astype(np.float64) ** 2).tolist()))  # double rounding
+
+
+def gain_folded_by_s(gamma, s_inv):
+    return (np.asarray(gamma, F32) / np.asarray(s_inv, F32)).astype(F32)           # times s
+
+
 ORIG = {name: getattr(O, name) for name in (
     "fold_quantize_weight", "smooth_factors", "calibrate_absmax", "_codes", "_scale_and_inverse",
     "quant_act", "w8a8_gemm", "static_act_scale", "act_quant_error", "weight_quant_error",
@@ -165,6 +182,9 @@ MUTATIONS = {
     "activation error ignores s^-1": ("act_quant_error", act_error_unscaled),
     "weight error scales rows": ("weight_quant_error", weight_error_transposed_scale),
     "difficulty uses the sample std": ("channel_stats", stats_sample_std),
+    "rms uses the sum of squares": ("rms_inverse", rms_without_mean),
+    "sum of squares rounded twice": ("sum_squares_f32", squares_rounded_through_float64),
+    "gain folded by s instead of 1/s": ("fold_norm_gain", gain_folded_by_s),
 }
 
 

@@ -470,3 +470,57 @@ def test_channel_stats_against_statistics_module():
     m2, sd2 = O.channel_stats(amax, scale)
     v = [float(F32(a * b)) for a, b in zip(amax, scale)]
     assert sd2 == pytest.approx(statistics.pstdev(v), rel=1e-12)
+
+
+
+# ---------------------------------------------------------------- RMSNorm fold
+def test_rms_inverse_against_high_precision():
+    """r_t is within 2 binary32 ulps of 1/sqrt(mean(h^2) + eps) computed with
+    200-bit arithmetic (five roundings of at most half an ulp each), and a
+    constant row of 2 with eps = 0 gives exactly 0.5."""
+    import mpmath
+    h = synth.normal(11, 1, 6 * 40, 1.0).reshape(6, 40).astype(F32)
+    h[2, :] = F32(-3.0)
+    h[4, 7] = F32(250.0)
+    eps = F32(1e-6)
+    r = O.rms_inverse(h, eps)
+    with mpmath.workprec(200):
+        for t in range(6):
+            ss = sum(mpmath.mpf(float(v)) ** 2 for v in h[t])
+            exact = float(1 / mpmath.sqrt(ss / 40 + mpmath.mpf(float(eps))))
+            assert abs(float(r[t]) - exact) <= 2 * float(np.spacing(F32(exact)))
+    assert O.rms_inverse(np.full((1, 64), 2.0, F32), F32(0.0))[0] == F32(0.5)
+
+
+def test_sum_of_squares_rounds_the_exact_sum():
+    """1 + 2^-24 + 2^-80: the float64 sum is the binary32 midpoint 1 + 2^-24
+    (ties to even would give 1), but the exact sum lies above it, so the
+    correctly rounded binary32 sum is 1 + 2^-23; the exact tie 1 + 2^-24
+    itself rounds to even (1)."""
+    row = np.array([1.0, 2.0 ** -12, 2.0 ** -40], F32)
+    assert O.sum_squares_f32(row) == F32(1.0 + 2.0 ** -23)
+    assert O.sum_squares_f32(np.array([1.0, 2.0 ** -12], F32)) == F32(1.0)
+    assert O.sum_squares_f32(np.array([3.0, -4.0], F32)) == F32(25.0)
+
+
+def test_folded_gain_matches_unfolded_path():
+    """Folding S^-1 into the gain changes only roundings: X' from the fold
+    is within 2 fp32 ulps of RMSNorm-then-X*S^-1, and in exact arithmetic
+    the folded layer equals the original X W (first page, paragraph 3)."""
+    c = synth.make_case("nf", 24, 64, 32, dtype="f32", outlier_frac=0.05, seed=12)
+    h = c.x_f32()
+    gamma = (0.5 + synth.uniform(12, 60, 64)).astype(F32)
+    eps = F32(1e-5)
+    r = O.rms_inverse(h, eps)
+    x = ((h * r[:, None]).astype(F32) * gamma[None, :]).astype(F32)      # RMSNorm output
+    ax, aw = O.calibrate_absmax(x, 0), O.calibrate_absmax(c.w_f32(), 1)
+    s, s_inv, _ = O.smooth_factors(ax, aw, 0.5)
+    _, _, _, xs_fold = O.rmsnorm_quant_act(h, O.fold_norm_gain(gamma, s_inv), eps, return_scaled=True)
+    _, _, _, xs_plain = O.quant_act(x, s_inv, return_scaled=True)
+    ulps = np.abs(xs_fold.view(np.int32).astype(np.int64) - xs_plain.view(np.int32).astype(np.int64))
+    assert ulps.max() <= 2
+    h64, g64, s64 = h.astype(np.float64), gamma.astype(np.float64), s.astype(np.float64)
+    rr = 1.0 / np.sqrt((h64 * h64).mean(axis=1) + float(eps))
+    y = ((h64 * rr[:, None]) * g64[None, :]) @ c.w_f32().astype(np.float64)
+    y_fold = ((h64 * rr[:, None]) * (g64 / s64)[None, :]) @ (s64[:, None] * c.w_f32().astype(np.float64))
+    assert np.linalg.norm(y_fold - y) / np.linalg.norm(y) <= 1e-12

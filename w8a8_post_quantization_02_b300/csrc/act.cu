@@ -59,20 +59,133 @@ SQ_DEVINL void load_sinv(const float* s_inv, int64_t e0, float* f) {
   }
 }
 
+constexpr int kDynamic = 0;  // per-token scale from the row's max|X'|
+constexpr int kStatic = 1;   // one calibrated scale for every token
+constexpr int kNorm = 2;     // RMS normalization with the folded gain, then per-token scale
+
+// 128-bit unsigned integer as (hi, lo).
+struct U128 {
+  uint64_t hi, lo;
+};
+SQ_DEVINL U128 add128(U128 a, U128 b) {
+  U128 r;
+  r.lo = a.lo + b.lo;
+  r.hi = a.hi + b.hi + (r.lo < a.lo ? 1ull : 0ull);
+  return r;
+}
+
+// Exact sums of squares as 128-bit fixed-point integers.  For h with
+// binary32 exponent field e (>= 1 after subnormals) and 24-bit significand
+// m, h^2 = m^2 * 2^(2e - 300).  A partial sum relative to exponent E holds
+// I = sum m^2 * 2^(62 - 2 (E - e)), i.e. sum h^2 = I * 2^(2E - 362); every
+// term is below 2^110, so a row of 32768 terms stays below 2^125.  Terms
+// more than 2^62 below the largest are truncated at the unit (relative
+// error below 2^-95: far under float64 resolution).
+SQ_DEVINL U128 shl128(uint64_t v, int sh) {  // v * 2^sh truncated, v < 2^48, sh <= 62
+  U128 r;
+  if (sh >= 0) {
+    r.lo = v << sh;
+    r.hi = sh ? (v >> (64 - sh)) : 0ull;
+  } else {
+    r.lo = (-sh < 64) ? (v >> (-sh)) : 0ull;
+    r.hi = 0ull;
+  }
+  return r;
+}
+
+SQ_DEVINL U128 shr128(U128 x, int sh) {  // x / 2^sh truncated, sh >= 0
+  if (sh == 0) return x;
+  U128 r;
+  if (sh >= 128) {
+    r.hi = r.lo = 0ull;
+  } else if (sh >= 64) {
+    r.lo = x.hi >> (sh - 64);
+    r.hi = 0ull;
+  } else {
+    r.lo = (x.lo >> sh) | (x.hi << (64 - sh));
+    r.hi = x.hi >> sh;
+  }
+  return r;
+}
+
+// Add h^2 for the element with |h| bits b to the sum I relative to exponent
+// E.  bf16-origin values (low 16 significand bits zero) within 2^15 of the
+// largest take a single 32 x 32 -> 64-bit multiply-add into the high word.
+template <bool BF16>
+SQ_DEVINL void add_square(U128& acc, uint32_t b, int E) {
+  const int e = (int)(b >> 23);
+  const int d2 = 2 * (E - (e ? e : 1));
+  if constexpr (BF16) {
+    const uint32_t m8 = ((b >> 16) & 0x7Fu) | (e ? 0x80u : 0u);
+    const uint32_t sq = m8 * m8;                 // < 2^16
+    if (d2 <= 30) {                              // sq * 2^(94 - d2): bits 64.. of the sum
+      const uint64_t add = (uint64_t)sq * (uint64_t)(1u << (30 - d2));
+      acc.hi += add;
+      return;
+    }
+    acc = add128(acc, shl128((uint64_t)sq << 32, 62 - d2));
+  } else {
+    const uint64_t m = (uint64_t)((b & 0x7FFFFFu) | (e ? 0x800000u : 0u));
+    acc = add128(acc, shl128(m * m, 62 - d2));
+  }
+}
+
+// I * 2^u rounded once to binary32 (nearest, ties to even; subnormal
+// results rounded at their own position, overflow to +inf).
+SQ_DEVINL float u128_scaled_to_f32(U128 x, int u) {
+  if (x.hi == 0 && x.lo == 0) return 0.0f;
+  const int t = x.hi ? 127 - __clzll((long long)x.hi) : 63 - __clzll((long long)x.lo);  // top bit
+  const int shift = max(t - 23, -149 - u);     // bits below `shift` are rounded off
+  if (shift <= 0) return ldexpf((float)x.lo, u);  // at most 24 significant bits: exact
+  // the sums held here stay below 2^125, so a shift of 128 or more means a
+  // value below 2^-152: under half the smallest subnormal
+  if (shift >= 128) return 0.0f;
+  const U128 q128 = shr128(x, shift);
+  uint32_t q = (uint32_t)q128.lo;              // < 2^24
+  // remainder against half a unit at `shift`
+  U128 rem;
+  if (shift >= 64) {
+    rem.hi = (shift == 64) ? 0ull : (x.hi & ((1ull << (shift - 64)) - 1ull));
+    rem.lo = x.lo;
+  } else {
+    rem.hi = 0ull;
+    rem.lo = x.lo & ((1ull << shift) - 1ull);
+  }
+  U128 half;
+  if (shift - 1 >= 64) {
+    half.hi = 1ull << (shift - 1 - 64);
+    half.lo = 0ull;
+  } else {
+    half.hi = 0ull;
+    half.lo = 1ull << (shift - 1);
+  }
+  const bool gt = rem.hi > half.hi || (rem.hi == half.hi && rem.lo > half.lo);
+  const bool eq = rem.hi == half.hi && rem.lo == half.lo;
+  if (gt || (eq && (q & 1u))) ++q;
+  return ldexpf((float)q, shift + u);          // q <= 2^24: exact scaling
+}
+
 // NT threads per CTA, each owning VPT 16-byte vectors of every row (vector
 // v = tid + i*NT).  With NT <= 512 the thread's s^-1 values stay in
 // registers; with 1024 threads (rows longer than 32 KiB) the register
 // budget is 64 per thread, so they are re-read through L1 for each row.
-// STATIC: one calibrated scale *d_static for every token instead of the
-// row maximum (no reduction; the clamp can act and `clipped` counts it).
-template <bool BF16, int CODES, int NT, int VPT, bool STATIC>
+// MODE kStatic: one calibrated scale *d_static for every token instead of
+// the row maximum (no reduction; the clamp can act and `clipped` counts it).
+// MODE kNorm: `s_inv` holds the folded gain gamma' and the row is first
+// RMS-normalized: the sum of squares is exact (128-bit fixed point,
+// order-independent) and rounded once to binary32, then
+// r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))) in IEEE binary32 and
+// X' = RN(RN(h * r) * gamma').  Two block barriers per row.
+template <bool BF16, int CODES, int NT, int VPT, int MODE>
 __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x, int64_t tokens,
                                                   int nvec, int64_t ldx_bytes,
                                                   const float* __restrict__ s_inv,
                                                   uint8_t* __restrict__ xq,
                                                   float* __restrict__ x_scale, int32_t* flags,
                                                   int stages, const float* __restrict__ d_static,
-                                                  uint32_t* clipped) {
+                                                  uint32_t* clipped, float eps) {
+  constexpr bool STATIC = MODE == kStatic;
+  constexpr bool NORM = MODE == kNorm;
   constexpr int E = BF16 ? 8 : 4;
   constexpr int NW = NT / 32;
   constexpr int CB = CODES == SQ_CODES_BF16 ? 2 : 1;
@@ -81,7 +194,10 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
   const uint32_t row_bytes = (uint32_t)nvec * 16u;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * row_bytes);
   uint32_t* red = reinterpret_cast<uint32_t*>(full + kMaxStages);  // [2][NW]
+  uint32_t* red_e = red + 2 * NW;                                    // [2][NW] (kNorm)
+  U128* red_s = reinterpret_cast<U128*>(full + kMaxStages + 2 * NW); // [2][NW] (kNorm)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cin = nvec * E;
 
   float si[kSiReg ? VPT : 1][E];
   if constexpr (kSiReg) {
@@ -130,11 +246,78 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
     // pass 1: X' = X * s^-1 into registers, and the thread's max|X'|
     float p[VPT][E];
     float m = 0.0f;
+    if constexpr (NORM) {
+      // the row into registers, the thread's largest binary32 exponent, and
+      // its exact sum of squares relative to that exponent
+      uint32_t tb = 0u;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = tid + i * NT;
-      if (ok && v < nvec) {
-        unpack<BF16>(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), p[i]);
+      for (int i = 0; i < VPT; ++i) {
+        const int v = tid + i * NT;
+        if (ok && v < nvec) {
+          unpack<BF16>(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), p[i]);
+#pragma unroll
+          for (int e = 0; e < E; ++e) tb = max(tb, __float_as_uint(p[i][e]) & 0x7FFFFFFFu);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) p[i][e] = 0.0f;
+        }
+      }
+      const int et = max(1, (int)(tb >> 23));  // 255: a non-finite value
+      U128 acc = {0ull, 0ull};
+      if (et < 255) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+#pragma unroll
+          for (int e = 0; e < E; ++e) add_square<BF16>(acc, __float_as_uint(p[i][e]) & 0x7FFFFFFFu, et);
+      }
+      // warp: align to the warp's largest exponent, then add (exact)
+      const int ew = (int)__reduce_max_sync(0xFFFFFFFFu, (uint32_t)et);
+      acc = shr128(acc, 2 * (ew - et));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        U128 other;
+        other.hi = __shfl_xor_sync(0xFFFFFFFFu, acc.hi, o);
+        other.lo = __shfl_xor_sync(0xFFFFFFFFu, acc.lo, o);
+        acc = add128(acc, other);
+      }
+      if (lane == 0) {
+        red_s[(it & 1) * NW + warp] = acc;
+        red_e[(it & 1) * NW + warp] = (uint32_t)ew;
+      }
+      if (__syncthreads_or(!ok)) {
+        aborted = true;
+        break;
+      }
+      if (tid == 0) {  // the row is in registers: refill the stage
+        const int64_t rn = r + (int64_t)stages * gridDim.x;
+        if (rn < tokens) {
+          mbar_expect_tx(&full[stage], row_bytes);
+          bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
+        }
+      }
+      // block: align the warps' sums to the row's largest exponent (every
+      // thread forms the same total in the same order)
+      int eb = 1;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) eb = max(eb, (int)red_e[(it & 1) * NW + w]);
+      const bool row_finite = eb < 255;
+      U128 tot = {0ull, 0ull};
+#pragma unroll
+      for (int w = 0; w < NW; ++w)
+        tot = add128(tot, shr128(red_s[(it & 1) * NW + w], 2 * (eb - (int)red_e[(it & 1) * NW + w])));
+      // r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))), S the exact sum rounded
+      // once to binary32, every step one IEEE binary32 operation
+      float rn32 = 0.0f;
+      if (row_finite && lane == 0) {
+        const float s32 = u128_scaled_to_f32(tot, 2 * eb - 362);
+        const float ms = __fadd_rn(__fdiv_rn(s32, (float)cin), eps);
+        rn32 = __fdiv_rn(1.0f, __fsqrt_rn(ms));
+      }
+      rn32 = __shfl_sync(0xFFFFFFFFu, rn32, 0);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = tid + i * NT;
+        if (!(v < nvec)) continue;
         float sv[E];
         if constexpr (kSiReg) {
 #pragma unroll
@@ -143,31 +326,56 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
           load_sinv<E>(s_inv, (int64_t)v * E, sv);
         }
 #pragma unroll
-        for (int e = 0; e < E; e += 2) mul2_rn(p[i][e], p[i][e + 1], sv[e], sv[e + 1]);
-        if constexpr (!STATIC) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) m = absmax_nan(m, p[i][e]);
+        for (int e = 0; e < E; e += 2) {
+          mul2_rn(p[i][e], p[i][e + 1], rn32, rn32);
+          mul2_rn(p[i][e], p[i][e + 1], sv[e], sv[e + 1]);
         }
-      } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) p[i][e] = 0.0f;
+        for (int e = 0; e < E; ++e) m = absmax_nan(m, row_finite ? p[i][e] : __int_as_float(0x7FFFFFFF));
       }
-    }
-    if constexpr (!STATIC) {
-      const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
-      if (lane == 0) red[(it & 1) * NW + warp] = mb;
-    }
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    // every thread has read this stage: refill it with the row `stages`
-    // iterations ahead
-    if (tid == 0) {
-      const int64_t rn = r + (int64_t)stages * gridDim.x;
-      if (rn < tokens) {
-        mbar_expect_tx(&full[stage], row_bytes);
-        bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
+      const uint32_t mbx = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
+      if (lane == 0) red[(it & 1) * NW + warp] = mbx;
+      __syncthreads();
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = tid + i * NT;
+        if (ok && v < nvec) {
+          unpack<BF16>(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), p[i]);
+          float sv[E];
+          if constexpr (kSiReg) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) sv[e] = si[i][e];
+          } else {
+            load_sinv<E>(s_inv, (int64_t)v * E, sv);
+          }
+#pragma unroll
+          for (int e = 0; e < E; e += 2) mul2_rn(p[i][e], p[i][e + 1], sv[e], sv[e + 1]);
+          if constexpr (!STATIC) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) m = absmax_nan(m, p[i][e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) p[i][e] = 0.0f;
+        }
+      }
+      if constexpr (!STATIC) {
+        const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
+        if (lane == 0) red[(it & 1) * NW + warp] = mb;
+      }
+      if (__syncthreads_or(!ok)) {
+        aborted = true;
+        break;
+      }
+      // every thread has read this stage: refill it with the row `stages`
+      // iterations ahead
+      if (tid == 0) {
+        const int64_t rn = r + (int64_t)stages * gridDim.x;
+        if (rn < tokens) {
+          mbar_expect_tx(&full[stage], row_bytes);
+          bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
+        }
       }
     }
     float d, inv;
@@ -268,15 +476,17 @@ struct ActLaunch {
 };
 
 struct Static {
-  const float* d;      // null: per-token scales
-  uint32_t* clipped;
+  int mode;            // kDynamic, kStatic or kNorm
+  const float* d;      // kStatic: the calibrated scale
+  uint32_t* clipped;   // kStatic: clip counter or null
+  float eps;           // kNorm
 };
 
-template <bool BF16, int CODES, int NT, int VPT, bool STATIC>
+template <bool BF16, int CODES, int NT, int VPT, int MODE>
 sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
                      const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags, Static sc,
                      cudaStream_t st) {
-  auto kern = k_quant_act<BF16, CODES, NT, VPT, STATIC>;
+  auto kern = k_quant_act<BF16, CODES, NT, VPT, MODE>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
@@ -287,26 +497,26 @@ sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_byt
   const size_t row_bytes = (size_t)nvec * 16;
   // about 64 KiB of rows in flight per CTA, at least two stages
   const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, 65536 / row_bytes));
-  const size_t smem = stages * row_bytes + kMaxStages * 8 + 2 * (NT / 32) * 4;
+  const size_t smem = stages * row_bytes + kMaxStages * 8 + 2 * (NT / 32) * (4 + 4 + 16) + 16;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NT, smem) != cudaSuccess)
     return SQ_ERR_CUDA;
   occ = std::max(1, std::min(occ, 4));
   const int64_t grid = std::min<int64_t>(tokens, (int64_t)sm_count() * occ);
   kern<<<(unsigned)grid, NT, smem, st>>>(x, tokens, nvec, ldx_bytes, s_inv, xq, x_scale, flags,
-                                         stages, sc.d, sc.clipped);
+                                         stages, sc.d, sc.clipped, sc.eps);
   return launch_status();
 }
 
-template <bool BF16, int CODES, int NT, bool STATIC>
+template <bool BF16, int CODES, int NT, int MODE>
 sq_status launch_act_vpt(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
                          const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
                          Static sc, cudaStream_t st) {
   switch ((nvec + NT - 1) / NT) {
-    case 1: return launch_act<BF16, CODES, NT, 1, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
-    case 2: return launch_act<BF16, CODES, NT, 2, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
-    case 3: return launch_act<BF16, CODES, NT, 3, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
-    case 4: return launch_act<BF16, CODES, NT, 4, STATIC>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case 1: return launch_act<BF16, CODES, NT, 1, MODE>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case 2: return launch_act<BF16, CODES, NT, 2, MODE>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case 3: return launch_act<BF16, CODES, NT, 3, MODE>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case 4: return launch_act<BF16, CODES, NT, 4, MODE>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
     default: return SQ_ERR_UNSUPPORTED;
   }
 }
@@ -315,8 +525,11 @@ template <bool BF16, int CODES, int NT>
 sq_status launch_act_nt(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_bytes,
                         const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags,
                         Static sc, cudaStream_t st) {
-  return sc.d ? launch_act_vpt<BF16, CODES, NT, true>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st)
-              : launch_act_vpt<BF16, CODES, NT, false>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+  switch (sc.mode) {
+    case kStatic: return launch_act_vpt<BF16, CODES, NT, kStatic>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    case kNorm: return launch_act_vpt<BF16, CODES, NT, kNorm>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+    default: return launch_act_vpt<BF16, CODES, NT, kDynamic>(nvec, x, tokens, ldx_bytes, s_inv, xq, x_scale, flags, sc, st);
+  }
 }
 
 template <bool BF16, int CODES>
@@ -360,13 +573,34 @@ int64_t quant_act_max_cin(sq_dtype dt) { return (int64_t)4096 * (dt == SQ_BF16 ?
 sq_status quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
                     const float* s_inv, void* xq, sq_codes fmt, float* x_scale, int32_t* flags,
                     cudaStream_t st) {
-  return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags, Static{nullptr, nullptr}, st);
+  return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags, Static{kDynamic, nullptr, nullptr, 0.0f}, st);
 }
 
 sq_status quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
                            const float* s_inv, const float* d, void* xq, sq_codes fmt,
                            float* x_scale, uint32_t* clipped, int32_t* flags, cudaStream_t st) {
-  return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags, Static{d, clipped}, st);
+  return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags, Static{kStatic, d, clipped, 0.0f}, st);
+}
+
+sq_status rmsnorm_quant_act(const void* h, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldh,
+                            const float* gamma_folded, float eps, void* xq, sq_codes fmt,
+                            float* x_scale, int32_t* flags, cudaStream_t st) {
+  return quant_act_any(h, dt, tokens, cin, ldh, gamma_folded, xq, fmt, x_scale, flags, Static{kNorm, nullptr, nullptr, eps}, st);
+}
+
+namespace {
+__global__ void k_fold_norm_gain(const float* __restrict__ gamma, const float* __restrict__ s_inv,
+                                 int64_t n, float* __restrict__ out) {
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n; j += (int64_t)gridDim.x * blockDim.x)
+    out[j] = __fmul_rn(gamma[j], s_inv[j]);
+}
+}  // namespace
+
+sq_status fold_norm_gain(const float* gamma, const float* s_inv, int64_t cin, float* out,
+                         cudaStream_t st) {
+  const int g = (int)std::min<int64_t>((cin + 255) / 256, 1024);
+  k_fold_norm_gain<<<g, 256, 0, st>>>(gamma, s_inv, cin, out);
+  return launch_status();
 }
 
 }  // namespace sq

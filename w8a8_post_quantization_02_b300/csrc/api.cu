@@ -12,6 +12,9 @@ sq_status quant_act(const void*, sq_dtype, int64_t, int64_t, int64_t, const floa
                     sq_codes, float*, int32_t*, cudaStream_t);
 int64_t quant_act_max_cin(sq_dtype);
 sq_status static_act_scale(const float*, const float*, int64_t, float*, int32_t*, cudaStream_t);
+sq_status fold_norm_gain(const float*, const float*, int64_t, float*, cudaStream_t);
+sq_status rmsnorm_quant_act(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, float,
+                            void*, sq_codes, float*, int32_t*, cudaStream_t);
 sq_status quant_act_static(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*,
                            const float*, void*, sq_codes, float*, uint32_t*, int32_t*, cudaStream_t);
 int fold_kernel_count(sq_dtype, int64_t, int64_t, int64_t);
@@ -79,6 +82,8 @@ int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int6
     case SQ_OP_QUANT_ACT: return 1;
     case SQ_OP_STATIC_SCALE: return 1;
     case SQ_OP_QUANT_ACT_STATIC: return 1;
+    case SQ_OP_FOLD_NORM_GAIN: return 1;
+    case SQ_OP_RMSNORM_QUANT_ACT: return 1;
     case SQ_OP_GEMM: return 1;
   }
   return -1;
@@ -149,6 +154,26 @@ sq_status sq_quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_
   if (cin > ((int64_t)1 << 30)) return SQ_ERR_UNSUPPORTED;
   return quant_act_static(x, dt, tokens, cin, ldx, s_inv, d, xq, fmt, x_scale, clipped, dev_flags,
                           stream);
+}
+
+sq_status sq_fold_norm_gain(const float* gamma, const float* s_inv, int64_t cin,
+                            float* gamma_folded, cudaStream_t stream) {
+  if (!gamma || !s_inv || !gamma_folded || cin < 1) return SQ_ERR_INVALID_ARG;
+  return fold_norm_gain(gamma, s_inv, cin, gamma_folded, stream);
+}
+
+sq_status sq_rmsnorm_quant_act(const void* h, sq_dtype dt, int64_t tokens, int64_t cin,
+                               int64_t ldh, const float* gamma_folded, float eps, void* xq,
+                               sq_codes fmt, float* x_scale, int32_t* dev_flags,
+                               cudaStream_t stream) {
+  if (!h || !gamma_folded || !xq || !x_scale || !valid_dtype(dt) || !valid_codes(fmt) || tokens < 1 ||
+      cin < 1 || ldh < cin || cin % 16 != 0 || !(eps >= 0.0f) || !(eps < 3.4e38f))
+    return SQ_ERR_INVALID_ARG;
+  if (!aligned16(h) || (ldh * elem_bytes(dt)) % 16 != 0 || !aligned16(xq) || !aligned16(gamma_folded))
+    return SQ_ERR_INVALID_ARG;
+  if (cin > quant_act_max_cin(dt)) return SQ_ERR_UNSUPPORTED;
+  return rmsnorm_quant_act(h, dt, tokens, cin, ldh, gamma_folded, eps, xq, fmt, x_scale, dev_flags,
+                           stream);
 }
 
 sq_status sq_act_quant_error(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,

@@ -26,8 +26,9 @@ def choose_codes(tokens: int) -> str:
 class Layer:
     def __init__(self, tokens: int, cin: int, cout: int, dtype: str, alpha: float,
                  codes: str | None = None, device="cuda", act_scale: str = "dynamic"):
-        if act_scale not in ("dynamic", "static"):
-            raise ValueError("act_scale is 'dynamic' (per token) or 'static' (one calibrated scale)")
+        if act_scale not in ("dynamic", "static", "norm"):
+            raise ValueError("act_scale is 'dynamic' (per token), 'static' (one calibrated scale) or "
+                             "'norm' (RMS normalization with S^-1 folded into its gain, then per token)")
         self.tokens, self.cin, self.cout = tokens, cin, cout
         self.dtype = dtype
         self.alpha = float(alpha)
@@ -51,6 +52,10 @@ class Layer:
         self.flags = torch.zeros(1, dtype=torch.int32, device=dv)
         self.d = torch.empty(1, dtype=torch.float32, device=dv)          # static scale
         self.clipped = torch.zeros(1, dtype=torch.int32, device=dv)      # static clip count
+        # 'norm' mode: x holds the normalization's input h, gamma its gain
+        self.gamma = torch.ones(cin, dtype=torch.float32, device=dv)
+        self.gamma_f = torch.empty(cin, dtype=torch.float32, device=dv)
+        self.eps = 1e-5
         fmt = sq._codes_fmt(self.codes)
         self._fmt = fmt
         ws_fold = sq.workspace_bytes(sq.SQ_OP_FOLD_QUANTIZE, 0, cout, cin, self.codes)
@@ -81,6 +86,8 @@ class Layer:
             "fold_quantize": K * N * eb + N * K * cb + N * 4,
             "quant_act": T * K * eb + T * K * cb + T * 4 + K * 4,
             "static_scale": K * 4 * 2 + 4,
+            "fold_norm_gain": K * 4 * 3,
+            "rmsnorm_quant_act": T * K * eb + T * K * cb + T * 4 + K * 4,
             "quant_act_static": T * K * eb + T * K * cb + T * 4 + K * 4,
             "gemm": (T + N) * K * cb + T * N * 2 + (T + N) * 4,
         }
@@ -133,8 +140,19 @@ class Layer:
                 ptr(self.x), dt, T, K, K, ptr(self.s_inv), ptr(self.d), ptr(self.xq), self._fmt,
                 ptr(self.x_scale), ptr(self.clipped), flags, st))
 
-        act = ([("quant_act", quant_act)] if self.act_scale == "dynamic"
-               else [("static_scale", static_scale), ("quant_act_static", quant_act_static)])
+        def fold_norm_gain(st):
+            ck("sq_fold_norm_gain", L.sq_fold_norm_gain(ptr(self.gamma), ptr(self.s_inv), K,
+                                                        ptr(self.gamma_f), st))
+
+        def rmsnorm_quant_act(st):
+            ck("sq_rmsnorm_quant_act", L.sq_rmsnorm_quant_act(
+                ptr(self.x), dt, T, K, K, ptr(self.gamma_f), self.eps, ptr(self.xq), self._fmt,
+                ptr(self.x_scale), flags, st))
+
+        act = {"dynamic": [("quant_act", quant_act)],
+               "static": [("static_scale", static_scale), ("quant_act_static", quant_act_static)],
+               "norm": [("fold_norm_gain", fold_norm_gain), ("rmsnorm_quant_act", rmsnorm_quant_act)],
+               }[self.act_scale]
         fns = ([("calibrate_x", calibrate_x), ("calibrate_w", calibrate_w), ("smooth", smooth),
                 ("fold_quantize", fold_quantize)] + act + [("gemm", gemm)])
         return [(name, counts[name], fn) for name, fn in fns]
@@ -151,6 +169,8 @@ class Layer:
             "quant_act": sq.kernel_count(sq.SQ_OP_QUANT_ACT, dt, T, 0, K, K),
             "static_scale": sq.kernel_count(sq.SQ_OP_STATIC_SCALE, dt, 0, 0, K),
             "quant_act_static": sq.kernel_count(sq.SQ_OP_QUANT_ACT_STATIC, dt, T, 0, K, K),
+            "fold_norm_gain": sq.kernel_count(sq.SQ_OP_FOLD_NORM_GAIN, dt, 0, 0, K),
+            "rmsnorm_quant_act": sq.kernel_count(sq.SQ_OP_RMSNORM_QUANT_ACT, dt, T, 0, K, K),
             "gemm": sq.kernel_count(sq.SQ_OP_GEMM, dt, T, N, K),
         }
 

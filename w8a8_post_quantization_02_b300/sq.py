@@ -20,7 +20,7 @@ SQ_FLAG_NONFINITE, SQ_FLAG_TIMEOUT = 1, 2
 SQ_F32, SQ_BF16 = 0, 1
 SQ_CODES_I8, SQ_CODES_BF16 = 0, 1
 (SQ_OP_CALIBRATE, SQ_OP_SMOOTH, SQ_OP_FOLD_QUANTIZE, SQ_OP_QUANT_ACT, SQ_OP_GEMM, SQ_OP_STATIC_SCALE,
- SQ_OP_QUANT_ACT_STATIC) = range(7)
+ SQ_OP_QUANT_ACT_STATIC, SQ_OP_FOLD_NORM_GAIN, SQ_OP_RMSNORM_QUANT_ACT) = range(9)
 
 # name -> (restype, argtypes), mirroring include/sq.h
 _P, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -31,6 +31,8 @@ SIGNATURES = {
     "sq_fold_quantize_weight_noalloc": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_static_act_scale": (_I32, [_P, _P, _I64, _P, _P, _P]),
+    "sq_fold_norm_gain": (_I32, [_P, _P, _I64, _P, _P]),
+    "sq_rmsnorm_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _F, _P, _I32, _P, _P, _P]),
     "sq_quant_act_static": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _P, _P, _P]),
     "sq_w8a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "sq_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64, _I32]),
@@ -204,6 +206,32 @@ def quant_act_static(x: torch.Tensor, s_inv: torch.Tensor, d: torch.Tensor, code
                                             _ptr(s_inv), _ptr(d), _ptr(xq), _codes_fmt(codes),
                                             _ptr(x_scale), _ptr(clipped), _ptr(flags), _stream(stream))
     _check("sq_quant_act_static", st)
+    return xq, x_scale
+
+
+def fold_norm_gain(gamma: torch.Tensor, s_inv: torch.Tensor, stream=None) -> torch.Tensor:
+    """Offline: the normalization gain with S^-1 folded in, gamma * (1/s)."""
+    out = torch.empty_like(gamma)
+    st = load_library().sq_fold_norm_gain(_ptr(gamma), _ptr(s_inv), gamma.numel(), _ptr(out),
+                                          _stream(stream))
+    _check("sq_fold_norm_gain", st)
+    return out
+
+
+def rmsnorm_quant_act(h: torch.Tensor, gamma_folded: torch.Tensor, eps: float, codes: str = "i8",
+                      flags: torch.Tensor | None = None, out=None, stream=None):
+    """RMS normalization with the folded gain fused into the per-token quantizer."""
+    _check_cuda_2d(h, "h")
+    tokens, cin = h.shape
+    if out is None:
+        xq = torch.empty(tokens, cin, device=h.device, dtype=_codes_dtype(codes))
+        x_scale = torch.empty(tokens, device=h.device, dtype=torch.float32)
+    else:
+        xq, x_scale = out
+    st = load_library().sq_rmsnorm_quant_act(_ptr(h), _dtype_code(h), tokens, cin, h.stride(0),
+                                             _ptr(gamma_folded), float(eps), _ptr(xq), _codes_fmt(codes),
+                                             _ptr(x_scale), _ptr(flags), _stream(stream))
+    _check("sq_rmsnorm_quant_act", st)
     return xq, x_scale
 
 
