@@ -78,7 +78,9 @@ typedef enum {
   SQ_OP_STATIC_SCALE = 5,
   SQ_OP_QUANT_ACT_STATIC = 6,
   SQ_OP_FOLD_NORM_GAIN = 7,
-  SQ_OP_RMSNORM_QUANT_ACT = 8
+  SQ_OP_RMSNORM_QUANT_ACT = 8,
+  SQ_OP_ROTATE_ACT = 9,
+  SQ_OP_ROTATE_WEIGHT = 10
 } sq_op;
 
 /*
@@ -246,6 +248,44 @@ sq_status sq_rmsnorm_quant_act(const void* h, sq_dtype dt, int64_t tokens, int64
                                int64_t ldh, const float* gamma_folded, float eps, void* xq,
                                sq_codes fmt, float* x_scale, int32_t* dev_flags,
                                cudaStream_t stream);
+
+/*
+ * Smooth Rotation (smoothing, then a Hadamard rotation, low-bit codes).
+ * Source: pith.science review of arXiv 2506.01967 ("Smooth Rotation"),
+ * key_machinery: X S^-1 R and R^T S W with the same Hadamard matrix R
+ * (entries +-1/sqrt(d)), which leaves Y = X W unchanged; core_discovery:
+ * symmetric round-to-nearest 4-bit codes on both operands (W4A4).
+ *
+ * R = H / sqrt(d) with H the Sylvester Hadamard matrix of order d = cin (a
+ * power of two).  Z = (X S^-1) H is formed by the fast Walsh-Hadamard
+ * transform, stages h = 1, 2, 4, ... in that order, each butterfly
+ * (a, b) -> (a + b, a - b) one binary32 addition and subtraction.  Codes
+ * clamp(rne(Z * (1/dz)), -qmax, qmax) with dz = RN(max|Z| / qmax) per row
+ * (1 if the maximum is 0); qmax = 7 gives 4-bit codes, 127 the 8-bit ones.
+ * The 1/d of R R^T = H H^T / d is carried by the activation scale as the
+ * exact factor 2^-log2(d): x_scale = dz * 2^-log2(d), w_scale = dz, so
+ * sq_w8a8_gemm reproduces the layer with its usual epilogue.
+ *
+ * sq_rotate_quant_act: x [tokens x cin] (ldx), s_inv device fp32 [cin] or
+ *   NULL (no smoothing), rotate 0/1 (0: plain per-token codes with qmax);
+ *   xq [tokens x cin] codes, x_scale device fp32 [tokens].
+ * sq_rotate_fold_quantize_weight: w [cin x cout] (ldw), s device fp32 [cin]
+ *   or NULL; wq [cout x cin] codes (K-major), w_scale device fp32 [cout];
+ *   workspace >= sq_workspace_bytes(SQ_OP_ROTATE_WEIGHT, 0, cout, cin, fmt)
+ *   (the folded weight, transposed, in fp32).
+ * Both: 1 <= qmax <= 127; with rotate = 1, cin a power of two with
+ * 256 <= cin <= 32768 (bf16) or 128 <= cin <= 16384 (fp32), else
+ * SQ_ERR_UNSUPPORTED; alignment as sq_quant_act.  A non-finite row maximum
+ * sets SQ_FLAG_NONFINITE.
+ */
+sq_status sq_rotate_quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                              const float* s_inv, int rotate, int qmax, void* xq, sq_codes fmt,
+                              float* x_scale, int32_t* dev_flags, cudaStream_t stream);
+sq_status sq_rotate_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin, int64_t cout,
+                                         int64_t ldw, const float* s, int rotate, int qmax,
+                                         void* wq, sq_codes fmt, float* w_scale,
+                                         int32_t* dev_flags, void* workspace, size_t ws_bytes,
+                                         cudaStream_t stream);
 
 /*
  * Step 5 - INT8 x INT8 GEMM with exact integer accumulation and a bf16

@@ -46,6 +46,8 @@ Readings where the pages are silent:
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 try:
@@ -462,6 +464,72 @@ def channel_stats(amax, scale=None):
 
 
 # --------------------------------------------------------------------------
+# Smooth Rotation: smoothing, then a Hadamard rotation, low-bit codes
+# --------------------------------------------------------------------------
+def fwht(v):
+    """Unnormalized fast Walsh-Hadamard transform along the last axis
+    (length a power of two), Sylvester ordering: stages h = 1, 2, 4, ...,
+    each butterfly (a, b) -> (a + b, a - b) one binary32 addition and one
+    subtraction.  Equals v @ H_d with H_d the Sylvester Hadamard matrix."""
+    x = np.array(v, dtype=F32, copy=True)
+    d = x.shape[-1]
+    assert d >= 1 and d & (d - 1) == 0, "length must be a power of two"
+    lead = x.shape[:-1]
+    h = 1
+    while h < d:
+        y = x.reshape(lead + (d // (2 * h), 2, h))
+        a, b = y[..., 0, :], y[..., 1, :]
+        x = np.stack(((a + b).astype(F32), (a - b).astype(F32)), axis=-2).reshape(lead + (d,))
+        h *= 2
+    return x
+
+
+def _rows_quantized(z, qmax):
+    """Per-row symmetric quantization with codes in [-qmax, qmax]: the
+    quantizer of reading 4 with 127 replaced by qmax."""
+    z = np.asarray(z, F32)
+    amax = np.max(np.abs(z), axis=1).astype(F32)
+    nonfinite = bool((~np.isfinite(amax)).any())
+    with np.errstate(invalid="ignore", over="ignore"):
+        d = (amax / F32(qmax)).astype(F32)
+        d = np.where(amax == 0, F32(1.0), d).astype(F32)
+        inv = (F32(1.0) / d).astype(F32)
+        t = (z * inv[:, None]).astype(F32)
+        r = np.clip(np.rint(t), -qmax, qmax)
+        r = np.where(np.isfinite(r), r, 0)
+    return r.astype(np.int8), d, nonfinite
+
+
+def rotate_quant_act(x, s_inv, rotate: bool, qmax: int):
+    """Smooth Rotation review (key_machinery): X S^-1 R with R = H_d / sqrt(d)
+    (entries +-1/sqrt(d)), then per-token symmetric codes with ``qmax``
+    (7 for 4 bits).  Z = fwht(X S^-1) is quantized unnormalized; the 1/d
+    of R R^T = H H^T / d is carried on the activation scale as the exact
+    power of two 2^-log2(d), so x_scale = RN(max|Z| / qmax) * 2^-log2(d)
+    and the GEMM epilogue is unchanged.  ``s_inv`` None: no smoothing;
+    ``rotate`` False: no rotation (and no 2^-log2(d))."""
+    x32 = np.asarray(x, F32)
+    xs = x32 if s_inv is None else (x32 * np.asarray(s_inv, F32)[None, :]).astype(F32)
+    z = fwht(xs) if rotate else xs
+    q, d, nonfinite = _rows_quantized(z, qmax)
+    if rotate:
+        d = np.ldexp(d, -int(round(math.log2(xs.shape[1])))).astype(F32)
+    return q, d, nonfinite
+
+
+def rotate_fold_quantize_weight(w, s, rotate: bool, qmax: int):
+    """R^T S W per output channel: the folded W'[j, n] = RN(s_j W[j, n]),
+    then for each output channel n the transform over j (fwht of the row n
+    of W'^T) and per-channel codes with ``qmax``.  Returns ``wq`` [Cout x
+    Cin], ``w_scale`` [Cout] (no power of two here: it rides on the
+    activation scale) and the non-finite flag."""
+    w32 = np.asarray(w, F32)
+    wf = w32 if s is None else (np.asarray(s, F32)[:, None] * w32).astype(F32)
+    zt = fwht(np.ascontiguousarray(wf.T)) if rotate else np.ascontiguousarray(wf.T)
+    return _rows_quantized(zt, qmax)
+
+
+# --------------------------------------------------------------------------
 # the whole path on one layer
 # --------------------------------------------------------------------------
 def run_path(x, w, alpha, rows=None):
@@ -489,7 +557,7 @@ __all__ = [
     "calibrate_absmax", "rn32_pow", "smooth_factors", "fold_quantize_weight", "quant_act",
     "static_act_scale", "quant_act_static", "act_quant_error", "weight_quant_error",
     "layer_error", "channel_stats", "fold_norm_gain", "sum_squares_f32", "rms_inverse",
-    "rmsnorm_quant_act",
+    "rmsnorm_quant_act", "fwht", "rotate_quant_act", "rotate_fold_quantize_weight",
     "int_accumulate", "bf16_rne_bits", "w8a8_gemm", "run_path", "bf16_ulp_distance",
     "STAT_FLOOR", "S_MIN", "S_MAX", "QMAX",
 ]

@@ -582,3 +582,80 @@ def test_rmsnorm_nonfinite_flag(sq):
     flags = flags_tensor()
     sq.rmsnorm_quant_act(h, torch.ones(64, device="cuda"), 1e-6, "i8", flags)
     assert int(flags.item()) & 1
+
+
+# ------------------------------------------------------------------ Smooth Rotation
+ROT_ACT_SHAPES = [(64, 512, "f32"), (37, 256, "bf16"), (300, 4096, "bf16"), (9, 8192, "f32"),
+                  (129, 16384, "bf16"), (40, 32768, "bf16"), (77, 11008, "bf16")]
+
+
+@pytest.mark.parametrize("qmax", [7, 127])
+@pytest.mark.parametrize("tokens,cin,dtype", ROT_ACT_SHAPES)
+def test_rotate_quant_act_bit_exact(sq, tokens, cin, dtype, qmax):
+    c = synth.make_case("ra", tokens, cin, 16, dtype=dtype, x_std=0.5, fixed_channels=2, fixed_factor=60.0,
+                        massive_tokens=min(3, tokens), massive_channels=2, seed=tokens + cin)
+    xf = c.x_f32()
+    si = (0.25 + 4.0 * synth.uniform(cin, 63, cin)).astype(F32)
+    pow2 = cin & (cin - 1) == 0
+    for smooth in (False, True):
+        for rotate in ((False, True) if pow2 else (False,)):
+            for codes in ("i8", "bf16"):
+                q_ref, xs_ref, nf = O.rotate_quant_act(xf, si if smooth else None, rotate, qmax)
+                flags = flags_tensor()
+                xq, xs = sq.rotate_quant_act(dev(c.x, dtype), torch.from_numpy(si).cuda() if smooth else None,
+                                             rotate, qmax, codes, flags)
+                assert int(flags.item()) == 0 and not nf
+                assert np.array_equal(f32bits(xs), npbits(xs_ref)), (smooth, rotate, codes)
+                assert np.array_equal(codes_np(xq), q_ref), (smooth, rotate, codes)
+
+
+ROT_W_SHAPES = [(256, 40, "bf16"), (4096, 264, "bf16"), (8192, 72, "bf16"), (512, 33, "f32"),
+                (11008, 24, "bf16")]
+
+
+@pytest.mark.parametrize("qmax", [7, 127])
+@pytest.mark.parametrize("cin,cout,dtype", ROT_W_SHAPES)
+def test_rotate_fold_quantize_weight_bit_exact(sq, cin, cout, dtype, qmax):
+    c = synth.make_case("rw", 1, cin, cout, dtype=dtype, w_std=0.02, seed=cin + cout)
+    s = (0.25 + 4.0 * synth.uniform(cin, 64, cin)).astype(F32)
+    pow2 = cin & (cin - 1) == 0
+    for smooth in (False, True):
+        for rotate in ((False, True) if pow2 else (False,)):
+            wq_ref, ws_ref, nf = O.rotate_fold_quantize_weight(c.w_f32(), s if smooth else None, rotate, qmax)
+            flags = flags_tensor()
+            wq, ws = sq.rotate_fold_quantize_weight(dev(c.w, dtype), torch.from_numpy(s).cuda() if smooth else None,
+                                                    rotate, qmax, "bf16", flags)
+            assert int(flags.item()) == 0 and not nf
+            assert np.array_equal(f32bits(ws), npbits(ws_ref)), (smooth, rotate)
+            assert np.array_equal(codes_np(wq), wq_ref), (smooth, rotate)
+
+
+def test_smooth_rotation_w4a4_layer_and_study(sq):
+    """W4A4 Smooth Rotation on a down_proj-like layer with massive outliers
+    (Cin = 8192, a power of two): the GEMM's accumulators are exact and Y is
+    within 1 ulp of the oracle; the four-way study's errors match the
+    oracle's."""
+    from w8a8_post_quantization_02_b300 import pipeline
+    c = synth.make_case("sr", 256, 8192, 512, dtype="bf16", x_std=0.5, w_std=0.02, alpha=0.5,
+                        fixed_channels=2, fixed_factor=60.0, massive_tokens=4, massive_channels=2, seed=21)
+    xf, wf = c.x_f32(), c.w_f32()
+    s_ref, si_ref, _ = O.smooth_factors(O.calibrate_absmax(xf, 0), O.calibrate_absmax(wf, 1), 0.5)
+    xq_ref, xs_ref, _ = O.rotate_quant_act(xf, si_ref, True, 7)
+    wq_ref, ws_ref, _ = O.rotate_fold_quantize_weight(wf, s_ref, True, 7)
+    acc_ref, y_ref = O.w8a8_gemm(xq_ref, xs_ref, wq_ref, ws_ref)
+    x_t, w_t = dev(c.x, "bf16"), dev(c.w, "bf16")
+    s_t, si_t = sq.smooth_factors(sq.calibrate_absmax(x_t, 0), sq.calibrate_absmax(w_t, 1), 0.5)
+    xq, xs = sq.rotate_quant_act(x_t, si_t, True, 7, "bf16")
+    wq, ws = sq.rotate_fold_quantize_weight(w_t, s_t, True, 7, "bf16")
+    y, acc = sq.w8a8_gemm(xq, xs, wq, ws, want_acc=True)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), acc_ref)
+    assert O.bf16_ulp_distance(y_bits(y), y_ref).max() <= 1
+    rows = np.arange(0, 256, 5)
+    study = pipeline.smooth_rotation_study(x_t, w_t, 0.5, 7, rows=torch.from_numpy(rows.astype(np.int32)))
+    for name, smooth, rotate in (("original", False, False), ("smooth", True, False),
+                                 ("rotate", False, True), ("smooth_rotate", True, True)):
+        xq_r, xs_r, _ = O.rotate_quant_act(xf, si_ref if smooth else None, rotate, 7)
+        wq_r, ws_r, _ = O.rotate_fold_quantize_weight(wf, s_ref if smooth else None, rotate, 7)
+        _, y_r = O.w8a8_gemm(xq_r, xs_r, wq_r, ws_r)
+        want = O.layer_error(xf, wf, y_r, rows).sum()
+        assert _rel_close(study[name]["layer_error"], want, 1e-3), name

@@ -41,6 +41,10 @@ def _pins():
         P.test_channel_stats_against_statistics_module,
         P.test_rms_inverse_against_high_precision,
         P.test_sum_of_squares_rounds_the_exact_sum,
+        P.test_fwht_is_the_sylvester_hadamard_product,
+        P.test_rotation_keeps_the_linear_map,
+        P.test_rotated_lone_outlier_maxima,
+        P.test_rotated_w4a4_codes_and_scales,
         P.test_folded_gain_matches_unfolded_path,
     ]
     for seed in range(6):
@@ -163,10 +167,33 @@ def gain_folded_by_s(gamma, s_inv):
     return (np.asarray(gamma, F32) / np.asarray(s_inv, F32)).astype(F32)           # times s
 
 
+def fwht_swapped_butterfly(v):
+    x = np.array(v, dtype=F32, copy=True)
+    d = x.shape[-1]
+    lead = x.shape[:-1]
+    h = 1
+    while h < d:
+        y = x.reshape(lead + (d // (2 * h), 2, h))
+        a, b = y[..., 0, :], y[..., 1, :]
+        x = np.stack(((a - b).astype(F32), (a + b).astype(F32)), axis=-2).reshape(lead + (d,))
+        h *= 2
+    return x
+
+
+def rotate_act_without_power_of_two(x, s_inv, rotate, qmax):
+    x32 = np.asarray(x, F32)
+    xs = x32 if s_inv is None else (x32 * np.asarray(s_inv, F32)[None, :]).astype(F32)
+    return O._rows_quantized(O.fwht(xs) if rotate else xs, qmax)
+
+
+def rows_quantized_qmax_plus_one(z, qmax):
+    return ORIG["_rows_quantized"](z, qmax + 1)
+
+
 ORIG = {name: getattr(O, name) for name in (
     "fold_quantize_weight", "smooth_factors", "calibrate_absmax", "_codes", "_scale_and_inverse",
     "quant_act", "w8a8_gemm", "static_act_scale", "act_quant_error", "weight_quant_error",
-    "channel_stats")}
+    "channel_stats", "_rows_quantized")}
 
 MUTATIONS = {
     "fold scales W's columns": ("fold_quantize_weight", fold_scales_columns),
@@ -184,6 +211,9 @@ MUTATIONS = {
     "difficulty uses the sample std": ("channel_stats", stats_sample_std),
     "rms uses the sum of squares": ("rms_inverse", rms_without_mean),
     "sum of squares rounded twice": ("sum_squares_f32", squares_rounded_through_float64),
+    "butterfly outputs swapped": ("fwht", fwht_swapped_butterfly),
+    "rotation drops 1/d": ("rotate_quant_act", rotate_act_without_power_of_two),
+    "low-bit grid off by one": ("_rows_quantized", rows_quantized_qmax_plus_one),
     "gain folded by s instead of 1/s": ("fold_norm_gain", gain_folded_by_s),
 }
 

@@ -524,3 +524,79 @@ def test_folded_gain_matches_unfolded_path():
     y = ((h64 * rr[:, None]) * g64[None, :]) @ c.w_f32().astype(np.float64)
     y_fold = ((h64 * rr[:, None]) * (g64 / s64)[None, :]) @ (s64[:, None] * c.w_f32().astype(np.float64))
     assert np.linalg.norm(y_fold - y) / np.linalg.norm(y) <= 1e-12
+
+
+
+# ---------------------------------------------------------------- Smooth Rotation
+def test_fwht_is_the_sylvester_hadamard_product():
+    """On integer vectors every butterfly is exact, so the transform equals
+    v @ H (scipy's Sylvester Hadamard matrix, integer arithmetic) exactly;
+    applying it twice gives d * v; on random floats it matches the float64
+    product within the rounding of log2(d) stages."""
+    from scipy.linalg import hadamard
+    for d in (1, 2, 8, 64, 256):
+        v = (np.floor(synth.uniform(d, 70, 3 * d) * 200) - 100).reshape(3, d).astype(F32)
+        H = hadamard(d).astype(np.int64)
+        assert np.array_equal(O.fwht(v).astype(np.int64), v.astype(np.int64) @ H)
+        assert np.array_equal(O.fwht(O.fwht(v)), (d * v).astype(F32))
+    d = 1024
+    v = synth.normal(5, 71, 4 * d, 1.0).reshape(4, d).astype(F32)
+    ref = v.astype(np.float64) @ hadamard(d).astype(np.float64)
+    assert np.abs(O.fwht(v) - ref).max() <= 10 * 2.0 ** -24 * np.abs(v).sum(axis=1).max()
+
+
+def test_rotation_keeps_the_linear_map():
+    """(X S^-1 R)(R^T S W) == X W to <= 1e-12 relative in float64 with
+    R = H / sqrt(d) orthogonal (Smooth Rotation review, key_machinery)."""
+    from scipy.linalg import hadamard
+    c = _small_case(K=64, N=32, alpha=0.5)
+    x, w = c.x_f32().astype(np.float64), c.w_f32().astype(np.float64)
+    s, _, _ = O.smooth_factors(O.calibrate_absmax(c.x_f32(), 0), O.calibrate_absmax(c.w_f32(), 1), 0.5)
+    R = hadamard(64).astype(np.float64) / 8.0
+    s64 = s.astype(np.float64)
+    y2 = ((x / s64) @ R) @ (R.T @ (s64[:, None] * w))
+    assert np.linalg.norm(y2 - x @ w) / np.linalg.norm(x @ w) <= 1e-12
+    assert np.allclose(R @ R.T, np.eye(64), atol=1e-15)
+
+
+def test_rotated_lone_outlier_maxima():
+    """A token that is zero except one outlier o: rotation spreads it to
+    +-o/sqrt(d) everywhere (review Eq (8) with one outlier); after smoothing
+    at alpha = 0.5 the outlier is sqrt(|o| max|W_j|) and the rotated maximum
+    is sqrt(|o| max|W_j|)/sqrt(d) -- the sqrt(d) denominator, not the
+    printed d of Eq (9) (the referee's correction)."""
+    d, j, o = 256, 37, F32(-900.0)
+    x = np.zeros((1, d), F32)
+    x[0, j] = o
+    z = O.fwht(x) / F32(16.0)
+    assert np.all(np.abs(z) == abs(o) / 16.0)
+    w = synth.normal(6, 72, d * 8, 0.02).reshape(d, 8).astype(F32)
+    aw = O.calibrate_absmax(w, 1)
+    ax = np.full(d, F32(1e-3))
+    ax[j] = abs(o)
+    s, s_inv, _ = O.smooth_factors(ax, aw, 0.5)
+    zs = O.fwht((x * s_inv[None, :]).astype(F32)) / F32(16.0)
+    want = math.sqrt(abs(float(o)) * float(aw[j])) / math.sqrt(d)
+    assert abs(float(np.abs(zs).max()) - want) <= 4 * float(np.spacing(F32(want)))
+
+
+def test_rotated_w4a4_codes_and_scales():
+    """4-bit codes stay in [-7, 7], each row's largest element maps to +-7,
+    the activation scale carries exactly 2^-log2(d), and a layer's codes
+    reproduce X W through the unchanged epilogue up to quantization error."""
+    c = synth.make_case("sr", 32, 128, 48, dtype="bf16", x_std=0.5, fixed_channels=2, fixed_factor=60.0,
+                        massive_tokens=3, massive_channels=2, seed=13)
+    x, w = c.x_f32(), c.w_f32()
+    s, s_inv, _ = O.smooth_factors(O.calibrate_absmax(x, 0), O.calibrate_absmax(w, 1), 0.5)
+    xq, xs, nf1 = O.rotate_quant_act(x, s_inv, True, 7)
+    wq, ws, nf2 = O.rotate_fold_quantize_weight(w, s, True, 7)
+    assert not (nf1 or nf2)
+    assert np.abs(xq).max() == 7 and np.abs(wq).max() == 7
+    assert all(np.abs(r).max() == 7 for r in xq) and all(np.abs(r).max() == 7 for r in wq)
+    z = O.fwht((x * s_inv[None, :]).astype(F32))
+    d_unscaled = (np.max(np.abs(z), axis=1) / F32(7)).astype(F32)
+    assert np.array_equal(xs, (d_unscaled / F32(128)).astype(F32))
+    acc, _ = O.w8a8_gemm(xq, xs, wq, ws)
+    yq = acc * xs.astype(np.float64)[:, None] * ws.astype(np.float64)[None, :]
+    y = x.astype(np.float64) @ w.astype(np.float64)
+    assert np.linalg.norm(yq - y) / np.linalg.norm(y) < 0.25

@@ -13,6 +13,11 @@ sq_status quant_act(const void*, sq_dtype, int64_t, int64_t, int64_t, const floa
 int64_t quant_act_max_cin(sq_dtype);
 sq_status static_act_scale(const float*, const float*, int64_t, float*, int32_t*, cudaStream_t);
 sq_status fold_norm_gain(const float*, const float*, int64_t, float*, cudaStream_t);
+bool rotate_len_ok(int64_t, sq_dtype, bool);
+sq_status rotate_quant_rows(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, bool, int,
+                            int, void*, sq_codes, float*, int32_t*, cudaStream_t);
+sq_status fold_transpose(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, float*,
+                         cudaStream_t);
 sq_status rmsnorm_quant_act(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, float,
                             void*, sq_codes, float*, int32_t*, cudaStream_t);
 sq_status quant_act_static(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*,
@@ -69,6 +74,7 @@ size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fm
   (void)fmt;
   switch (op) {
     case SQ_OP_FOLD_QUANTIZE: return n > 0 ? round256((size_t)n * 4) : 0;
+    case SQ_OP_ROTATE_WEIGHT: return (n > 0 && k > 0) ? round256((size_t)n * (size_t)k * 4) : 0;
     default: return 0;
   }
 }
@@ -84,6 +90,8 @@ int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int6
     case SQ_OP_QUANT_ACT_STATIC: return 1;
     case SQ_OP_FOLD_NORM_GAIN: return 1;
     case SQ_OP_RMSNORM_QUANT_ACT: return 1;
+    case SQ_OP_ROTATE_ACT: return 1;
+    case SQ_OP_ROTATE_WEIGHT: return 2;
     case SQ_OP_GEMM: return 1;
   }
   return -1;
@@ -174,6 +182,41 @@ sq_status sq_rmsnorm_quant_act(const void* h, sq_dtype dt, int64_t tokens, int64
   if (cin > quant_act_max_cin(dt)) return SQ_ERR_UNSUPPORTED;
   return rmsnorm_quant_act(h, dt, tokens, cin, ldh, gamma_folded, eps, xq, fmt, x_scale, dev_flags,
                            stream);
+}
+
+sq_status sq_rotate_quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                              const float* s_inv, int rotate, int qmax, void* xq, sq_codes fmt,
+                              float* x_scale, int32_t* dev_flags, cudaStream_t stream) {
+  if (!x || !xq || !x_scale || !valid_dtype(dt) || !valid_codes(fmt) || tokens < 1 || cin < 1 ||
+      ldx < cin || cin % 16 != 0 || qmax < 1 || qmax > 127 || (rotate != 0 && rotate != 1))
+    return SQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || (ldx * elem_bytes(dt)) % 16 != 0 || !aligned16(xq) || (s_inv && !aligned16(s_inv)))
+    return SQ_ERR_INVALID_ARG;
+  if (!rotate_len_ok(cin, dt, rotate != 0)) return SQ_ERR_UNSUPPORTED;
+  int l2 = 0;
+  while ((1LL << l2) < cin) ++l2;
+  return rotate_quant_rows(x, dt, tokens, cin, ldx, s_inv, rotate != 0, qmax, rotate ? l2 : 0, xq, fmt,
+                           x_scale, dev_flags, stream);
+}
+
+sq_status sq_rotate_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin, int64_t cout,
+                                         int64_t ldw, const float* s, int rotate, int qmax,
+                                         void* wq, sq_codes fmt, float* w_scale,
+                                         int32_t* dev_flags, void* workspace, size_t ws_bytes,
+                                         cudaStream_t stream) {
+  if (!w || !wq || !w_scale || !valid_dtype(dt) || !valid_codes(fmt) || cin < 1 || cout < 1 ||
+      ldw < cout || cin % 16 != 0 || qmax < 1 || qmax > 127 || (rotate != 0 && rotate != 1))
+    return SQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w) % elem_bytes(dt)) != 0 || !aligned16(wq)) return SQ_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < sq_workspace_bytes(SQ_OP_ROTATE_WEIGHT, 0, cout, cin, fmt) ||
+      !aligned16(workspace))
+    return SQ_ERR_WORKSPACE;
+  if (!rotate_len_ok(cin, SQ_F32, rotate != 0)) return SQ_ERR_UNSUPPORTED;
+  float* wt = static_cast<float*>(workspace);
+  const sq_status st = fold_transpose(w, dt, cin, cout, ldw, s, wt, stream);
+  if (st != SQ_OK) return st;
+  return rotate_quant_rows(wt, SQ_F32, cout, cin, cin, nullptr, rotate != 0, qmax, 0, wq, fmt, w_scale,
+                           dev_flags, stream);
 }
 
 sq_status sq_act_quant_error(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,

@@ -253,3 +253,31 @@ def alpha_sweep(x: torch.Tensor, w: torch.Tensor, alphas, codes: str | None = No
         results.append(diagnose(layer, rows))
     torch.cuda.synchronize()
     return results
+
+
+def smooth_rotation_study(x: torch.Tensor, w: torch.Tensor, alpha: float = 0.5, qmax: int = 7,
+                          codes: str = "bf16", rows=None) -> dict:
+    """The four preprocessing choices the Smooth Rotation review compares,
+    each quantized to +-qmax codes on both operands (qmax = 7: W4A4) and run
+    through the same GEMM: 'original', 'smooth', 'rotate', 'smooth_rotate'.
+    Returns each one's layer error (sum over the sampled tokens of the
+    squared difference to the unquantized X W) and its activation-scale
+    maximum.  Cin must be a power of two for the rotated variants."""
+    tokens, cin = x.shape
+    if rows is None:
+        n = min(64, tokens)
+        rows = torch.linspace(0, tokens - 1, n).round().to(torch.int32)
+    rows = torch.as_tensor(rows, dtype=torch.int32)
+    amax_x = sq.calibrate_absmax(x, 0)
+    amax_w = sq.calibrate_absmax(w, 1)
+    s, s_inv = sq.smooth_factors(amax_x, amax_w, alpha)
+    out = {}
+    for name, smooth, rotate in (("original", False, False), ("smooth", True, False),
+                                 ("rotate", False, True), ("smooth_rotate", True, True)):
+        xq, xs = sq.rotate_quant_act(x, s_inv if smooth else None, rotate, qmax, codes)
+        wq, ws = sq.rotate_fold_quantize_weight(w, s if smooth else None, rotate, qmax, codes)
+        y = sq.w8a8_gemm(xq, xs, wq, ws)
+        err = sq.layer_error(x, w, y, rows)
+        out[name] = {"layer_error": float(err.sum()), "x_scale_max": float(xs.max())}
+    torch.cuda.synchronize()
+    return out

@@ -20,7 +20,8 @@ SQ_FLAG_NONFINITE, SQ_FLAG_TIMEOUT = 1, 2
 SQ_F32, SQ_BF16 = 0, 1
 SQ_CODES_I8, SQ_CODES_BF16 = 0, 1
 (SQ_OP_CALIBRATE, SQ_OP_SMOOTH, SQ_OP_FOLD_QUANTIZE, SQ_OP_QUANT_ACT, SQ_OP_GEMM, SQ_OP_STATIC_SCALE,
- SQ_OP_QUANT_ACT_STATIC, SQ_OP_FOLD_NORM_GAIN, SQ_OP_RMSNORM_QUANT_ACT) = range(9)
+ SQ_OP_QUANT_ACT_STATIC, SQ_OP_FOLD_NORM_GAIN, SQ_OP_RMSNORM_QUANT_ACT, SQ_OP_ROTATE_ACT,
+ SQ_OP_ROTATE_WEIGHT) = range(11)
 
 # name -> (restype, argtypes), mirroring include/sq.h
 _P, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -32,6 +33,9 @@ SIGNATURES = {
     "sq_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_static_act_scale": (_I32, [_P, _P, _I64, _P, _P, _P]),
     "sq_fold_norm_gain": (_I32, [_P, _P, _I64, _P, _P]),
+    "sq_rotate_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _I32, _I32, _P, _I32, _P, _P, _P]),
+    "sq_rotate_fold_quantize_weight": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _I32, _I32, _P, _I32, _P,
+                                              _P, _P, _SZ, _P]),
     "sq_rmsnorm_quant_act": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _F, _P, _I32, _P, _P, _P]),
     "sq_quant_act_static": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _P, _I32, _P, _P, _P, _P]),
     "sq_w8a8_gemm": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
@@ -233,6 +237,39 @@ def rmsnorm_quant_act(h: torch.Tensor, gamma_folded: torch.Tensor, eps: float, c
                                              _ptr(x_scale), _ptr(flags), _stream(stream))
     _check("sq_rmsnorm_quant_act", st)
     return xq, x_scale
+
+
+def rotate_quant_act(x: torch.Tensor, s_inv: torch.Tensor | None, rotate: bool = True, qmax: int = 7,
+                     codes: str = "i8", flags: torch.Tensor | None = None, stream=None):
+    """Smooth Rotation, activation side: codes of (X S^-1) H per token with
+    grid +-qmax; x_scale carries 2^-log2(cin) when rotated."""
+    _check_cuda_2d(x, "x")
+    tokens, cin = x.shape
+    xq = torch.empty(tokens, cin, device=x.device, dtype=_codes_dtype(codes))
+    x_scale = torch.empty(tokens, device=x.device, dtype=torch.float32)
+    st = load_library().sq_rotate_quant_act(_ptr(x), _dtype_code(x), tokens, cin, x.stride(0), _ptr(s_inv),
+                                            int(rotate), int(qmax), _ptr(xq), _codes_fmt(codes),
+                                            _ptr(x_scale), _ptr(flags), _stream(stream))
+    _check("sq_rotate_quant_act", st)
+    return xq, x_scale
+
+
+def rotate_fold_quantize_weight(w: torch.Tensor, s: torch.Tensor | None, rotate: bool = True,
+                                qmax: int = 7, codes: str = "i8", flags: torch.Tensor | None = None,
+                                workspace: torch.Tensor | None = None, stream=None):
+    """Smooth Rotation, weight side: codes of H^T S W per output channel."""
+    _check_cuda_2d(w, "w")
+    cin, cout = w.shape
+    wq = torch.empty(cout, cin, device=w.device, dtype=_codes_dtype(codes))
+    w_scale = torch.empty(cout, device=w.device, dtype=torch.float32)
+    nbytes = workspace_bytes(SQ_OP_ROTATE_WEIGHT, 0, cout, cin, codes)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), device=w.device, dtype=torch.uint8)
+    st = load_library().sq_rotate_fold_quantize_weight(
+        _ptr(w), _dtype_code(w), cin, cout, w.stride(0), _ptr(s), int(rotate), int(qmax), _ptr(wq),
+        _codes_fmt(codes), _ptr(w_scale), _ptr(flags), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("sq_rotate_fold_quantize_weight", st)
+    return wq, w_scale
 
 
 def w8a8_gemm(xq: torch.Tensor, x_scale: torch.Tensor, wq: torch.Tensor, w_scale: torch.Tensor,
