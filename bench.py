@@ -233,8 +233,6 @@ def to_device(case, torch):
 # on the same workload (dram__bytes_read.sum + dram__bytes_write.sum), or
 # absent when the kernel changed after the capture.
 NCU_TRAFFIC_BYTES = {
-    # 109.45 MB read + 25.58 MB written (the rest of Y still dirty in L2)
-    ("k_gemm_bf16c", "prefill_upgate_2048x4096x11008"): 135.03e6,
 }
 
 

@@ -274,7 +274,7 @@ def test_gemm_shapes_random_codes(sq, codes, m, n, k):
 # 896-row CTAs), strips cut short by Cout, fp32 weights, and Cin beyond the
 # single-pass limit (the two-pass path).
 FOLD_SHAPES = [
-    (768, 40, "bf16"), (1536, 96, "bf16"), (1552, 40, "bf16"), (4096, 264, "bf16"),
+    (768, 40, "bf16"), (1536, 96, "bf16"), (1552, 40, "bf16"), (4096, 264, "bf16"), (6144, 136, "bf16"),
     (6160, 72, "bf16"), (12288, 32, "bf16"), (12304, 24, "bf16"), (2048, 20, "f32"),
     (48, 1000, "f32"),
 ]

@@ -87,9 +87,13 @@ SQ_DEVINL bool mbar_try_wait(uint64_t* b, uint32_t parity) { return async::mbar_
 SQ_DEVINL uint64_t global_ns() { return async::global_ns(); }
 
 // Arrive on an mbarrier given by its shared::cluster address (this CTA's
-// or the peer's).
+// or the peer's).  The barriers this is used on order tensor-memory reads
+// (completed by tcgen05.wait::ld, fenced by tcgen05.fence around the
+// arrive/wait pair) before the MMAs that overwrite the same columns; no
+// generic-memory data passes through them, so the default CTA-scope release
+// is enough (a cluster-scope release costs a memory barrier per arrive).
 SQ_DEVINL void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
 // Bounded wait for the phase with parity `parity` to complete.  Returns

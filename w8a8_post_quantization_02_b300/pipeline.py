@@ -179,28 +179,54 @@ class Layer:
         counts = self.kernel_counts()
         return sum(counts[name] for name, _, _ in self.stages())
 
+    def _enqueue(self, fns: dict, main, side) -> None:
+        """Enqueue steps 1-4 on two streams.  The X side (absmax of X, then
+        the activation codes) runs on ``side`` beside the W side (absmax of W,
+        then the fold); they meet at the smoothing factors, which need both
+        absmax vectors, and again before the GEMM.  Same kernels and work as
+        the serial order, fewer idle SMs in the small kernels and tails."""
+        act = [n for n in fns if n not in ("calibrate_x", "calibrate_w", "smooth", "fold_quantize", "gemm")]
+        fork, x_done, s_done, act_done = (torch.cuda.Event() for _ in range(4))
+        fork.record(main)
+        side.wait_event(fork)
+        fns["calibrate_x"](sq._stream(side))
+        x_done.record(side)
+        fns["calibrate_w"](sq._stream(main))
+        main.wait_event(x_done)
+        fns["smooth"](sq._stream(main))
+        s_done.record(main)
+        side.wait_event(s_done)
+        for name in act:
+            fns[name](sq._stream(side))
+        act_done.record(side)
+        fns["fold_quantize"](sq._stream(main))
+        main.wait_event(act_done)
+
+    def _side_stream(self):
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(device=self.x.device)
+        return self._side
+
     def step(self, want_acc: bool = False, stream=None) -> None:
-        st = sq._stream(stream)
-        for _, _, fn in self.stages(want_acc):
-            fn(st)
+        main = stream if stream is not None else torch.cuda.current_stream()
+        fns = {name: fn for name, _, fn in self.stages(want_acc)}
+        self._enqueue(fns, main, self._side_stream())
+        fns["gemm"](sq._stream(main))
 
     def capture(self, want_acc: bool = False):
         """Two CUDA graphs of one step: steps 1-4 (calibration through the
-        activation codes) and the GEMM, replayed with ``graph.replay()`` on
-        the current stream.  Call ``step()`` once first, outside capture, so
-        the library's one-time set-up (kernel attributes) is done."""
-        stages = self.stages(want_acc)
-        pre = [fn for name, _, fn in stages if name != "gemm"]
-        gemm = [fn for name, _, fn in stages if name == "gemm"]
-        graphs = []
-        for fns in (pre, gemm):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                st = sq._stream()
-                for fn in fns:
-                    fn(st)
-            graphs.append(g)
-        return graphs[0], graphs[1]
+        activation codes, forked over two streams and joined) and the GEMM,
+        replayed with ``graph.replay()`` on the current stream.  Call
+        ``step()`` once first, outside capture, so the library's one-time
+        set-up (kernel attributes) is done."""
+        fns = {name: fn for name, _, fn in self.stages(want_acc)}
+        side = self._side_stream()
+        g_pre, g_gemm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_pre):
+            self._enqueue(fns, torch.cuda.current_stream(), side)
+        with torch.cuda.graph(g_gemm):
+            fns["gemm"](sq._stream())
+        return g_pre, g_gemm
 
 
 def available_codes():
