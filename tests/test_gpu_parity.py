@@ -253,7 +253,11 @@ def test_gemm_saturated_widest_k(sq, codes):
     # valid rows (M = 300), K tails inside a k-block and several
     # 1024-product chunks
     (129, 72, 80), (520, 3080, 272), (777, 3464, 1040), (777, 4040, 2064), (2048, 2168, 208),
-    (300, 1000, 3088)])
+    (300, 1000, 3088),
+    # int8 codes: weight rows staged in shared memory up to K = 12288 (a
+    # ragged last block of rows, M in each of the 16/32/64-token tilings),
+    # the register-fed kernel beyond it
+    (16, 4104, 4096), (33, 40, 12288), (5, 24, 12304)])
 def test_gemm_shapes_random_codes(sq, codes, m, n, k):
     u = synth.uniform(m + n + k, 5, (m + n) * k)
     codes_all = np.clip(np.floor(u * 255.0) - 127.0, -127, 127).astype(np.int8)
