@@ -362,7 +362,9 @@ def run_ours(args, case_name):
         "parallelism": f"replicas x{world}",
     }
     if not args.no_e2e:
-        line["e2e"] = run_e2e(layer, g_pre, g_gemm, x_host, w_host, args.e2e_steps, ops, world, torch)
+        if args.act_scale == "dynamic":
+            layers = [layer, pipeline.Layer.for_case(case, codes=layer.codes)]
+            line["e2e"] = run_e2e(layers, x_host, w_host, args.e2e_steps, ops, world, torch)
     if rank == 0 and not args.no_cpu_baseline:
         times, o_ops = time_oracle(case, 20.0, min(case.tokens, 256), 3)
         line["cpu_baseline"] = {"value": o_ops * len(times) / sum(times) / 1e12, "unit": "TOPS",
@@ -374,34 +376,72 @@ def run_ours(args, case_name):
     return 0
 
 
-def run_e2e(layer, g_pre, g_gemm, x_host, w_host, steps, ops, world, torch):
-    """Same metric through the public API with host buffers: pinned-host
-    H2D of X and W, the whole path, and D2H of Y, every step."""
+def gpu_local_cpus(torch, device):
+    """The CPUs of the GPU's NUMA node (from sysfs) that this process may
+    use, or None when that cannot be read."""
+    try:
+        p = torch.cuda.get_device_properties(device)
+        path = (f"/sys/bus/pci/devices/{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:"
+                f"{p.pci_device_id:02x}.0/local_cpulist")
+        cpus = set()
+        for part in open(path).read().strip().split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return cpus or None
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
+def run_e2e(layers, x_host, w_host, steps, ops, world, torch):
+    """Same metric through the C ABI with host buffers: every step is one
+    sq_linear_host call (X and W copied in from pinned host memory, the whole
+    path, Y copied out to pinned host memory).  Steps alternate between two
+    streams, each with its own device buffers and host Y, so one step's
+    copies overlap the other step's copies in the opposite direction and its
+    kernels."""
+    # page-locked host buffers on the GPU's NUMA node: the pages are placed
+    # where the pinning thread runs, and copies from a far node were measured
+    # at less than half the near node's rate
+    local = gpu_local_cpus(torch, torch.cuda.current_device())
+    saved = os.sched_getaffinity(0)
+    if local:
+        os.sched_setaffinity(0, local)
     xh, wh = x_host.pin_memory(), w_host.pin_memory()
-    yh = torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()
-    stream = torch.cuda.current_stream()
+    yh = [torch.empty(layers[0].y.shape, dtype=torch.bfloat16).pin_memory() for _ in layers]
+    streams = [torch.cuda.Stream() for _ in layers]
+    bufs = [lay.linear_buffers() for lay in layers]
 
-    def step():
-        layer.x.copy_(xh, non_blocking=True)
-        layer.w.copy_(wh, non_blocking=True)
-        g_pre.replay()
-        g_gemm.replay()
-        yh.copy_(layer.y, non_blocking=True)
+    def step(i):
+        j = i % len(layers)
+        layers[j].run_host(xh, wh, yh[j], stream=streams[j], bufs=bufs[j])
 
-    for _ in range(2):
-        step()
+    for i in range(2 * len(layers)):
+        step(i)
     torch.cuda.synchronize()
+    main = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(main)
+    for st in streams:
+        st.wait_event(e0)
+    for i in range(steps):
+        step(i)
+    for st in streams:
+        main.wait_stream(st)
+    e1.record(main)
     torch.cuda.synchronize()
+    for lay in layers:
+        if int(lay.flags.item()) != 0:
+            raise RuntimeError(f"device flags raised during the end-to-end steps: {int(lay.flags.item())}")
+    if local:
+        os.sched_setaffinity(0, saved)
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     return {"value": world * steps * ops / (ms * 1e-3) / 1e12, "unit": "TOPS",
+            "host_buffers": ("page-locked, on the GPU's NUMA node" if local else "page-locked"),
             "h2d_bytes_per_step": xh.numel() * xh.element_size() + wh.numel() * wh.element_size(),
-            "d2h_bytes_per_step": yh.numel() * yh.element_size()}
+            "d2h_bytes_per_step": yh[0].numel() * yh[0].element_size(),
+            "api": "sq_linear_host (C ABI, host buffers), two streams alternating"}
 
 
 def main():

@@ -351,6 +351,53 @@ sq_status sq_layer_error(const void* x, const void* w, sq_dtype dt, int64_t toke
 sq_status sq_channel_stats(const float* amax, const float* scale, int64_t n, double* out,
                            cudaStream_t stream);
 
+/*
+ * The whole path on host-resident inputs, one call per layer.  No source
+ * page defines this call; it is the end-to-end form of steps 1-5 above for
+ * callers whose X and W live in host memory.  Enqueued on `stream`, in this
+ * order: copy X and W from host to the caller's device buffers; step 1 on X
+ * (axis 0) and on W (axis 1); step 2 with strength alpha; step 3; step 4
+ * (dynamic per-token scale); step 5 without the accumulators; copy Y back
+ * to host memory.  Every intermediate stays in `dev` for the caller.
+ *   x_host  host [tokens x cin], type dt, contiguous
+ *   w_host  host [cin x cout], type dt, contiguous
+ *   y_host  host bf16 [tokens x cout], contiguous
+ *   dev     host pointer to the caller's device buffers (layouts and formats
+ *           as in steps 1-5, all contiguous): x, w as above; amax_x,
+ *           amax_w, s, s_inv fp32 [cin]; wq [cout x cin] and xq
+ *           [tokens x cin] codes in format fmt; w_scale fp32 [cout];
+ *           x_scale fp32 [tokens]; y bf16 [tokens x cout]; workspace of at
+ *           least sq_workspace_bytes(SQ_OP_FOLD_QUANTIZE, 0, cout, cin, fmt)
+ *   dev_flags  device int32 or NULL, as in the steps
+ * The copies are asynchronous only from page-locked host memory
+ * (cudaHostAlloc or cudaHostRegister); from pageable memory CUDA stages them
+ * and the call may block.  The host buffers must stay valid, and y_host
+ * unread, until `stream` has finished the call's work.  All arguments are
+ * checked before anything is enqueued (cin a multiple of 16, x, xq and wq
+ * 16-byte aligned, every other buffer 4-byte aligned, cin within step 4's
+ * limit); a failing copy or launch returns SQ_ERR_CUDA with the earlier
+ * work of the call already enqueued.
+ */
+typedef struct {
+  void* x;
+  void* w;
+  float* amax_x;
+  float* amax_w;
+  float* s;
+  float* s_inv;
+  void* wq;
+  float* w_scale;
+  void* xq;
+  float* x_scale;
+  void* y;
+  void* workspace;
+  size_t ws_bytes;
+} sq_linear_buffers;
+
+sq_status sq_linear_host(const void* x_host, const void* w_host, sq_dtype dt, int64_t tokens,
+                         int64_t cin, int64_t cout, float alpha, sq_codes fmt, void* y_host,
+                         const sq_linear_buffers* dev, int32_t* dev_flags, cudaStream_t stream);
+
 /* Workspace bytes an operation needs for these sizes (0 if none). */
 size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fmt);
 

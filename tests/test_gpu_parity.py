@@ -389,6 +389,41 @@ def test_full_workload_parity(sq, name):
     assert O.bf16_ulp_distance(y, y_ref).max() <= 1
 
 
+# ------------------------------------------------------------------ whole path from host memory
+@pytest.mark.parametrize("name,codes", [("single_linear_64x512x512", None), ("decode_7b_16x4096x4096", None),
+                                        ("decode_7b_16x4096x4096", "bf16")])
+def test_linear_host_parity(sq, name, codes):
+    """sq_linear_host: pinned host X and W in, host Y out, through the C ABI;
+    every intermediate bit-exact against the oracle, Y within 1 bf16 ulp."""
+    from w8a8_post_quantization_02_b300 import pipeline
+    c = synth.workload(name)
+    ref_ax = O.calibrate_absmax(c.x_f32(), 0)
+    ref_aw = O.calibrate_absmax(c.w_f32(), 1)
+    s_ref, si_ref, _ = O.smooth_factors(ref_ax, ref_aw, c.alpha)
+    wq_ref, ws_ref, _ = O.fold_quantize_weight(c.w_f32(), s_ref)
+    xq_ref, xs_ref, _ = O.quant_act(c.x_f32(), si_ref)
+    _, y_ref = O.w8a8_gemm(xq_ref, xs_ref, wq_ref, ws_ref)
+
+    layer = pipeline.Layer.for_case(c, codes=codes)
+    x_host = dev(c.x, c.dtype).cpu().pin_memory()
+    w_host = dev(c.w, c.dtype).cpu().pin_memory()
+    y_host = torch.empty(c.tokens, c.cout, dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.Stream()
+    layer.run_host(x_host, w_host, y_host, stream=stream)
+    stream.synchronize()
+    assert int(layer.flags.item()) == 0
+    assert np.array_equal(f32bits(layer.amax_x), npbits(ref_ax))
+    assert np.array_equal(f32bits(layer.amax_w), npbits(ref_aw))
+    assert np.array_equal(f32bits(layer.s), npbits(s_ref))
+    assert np.array_equal(codes_np(layer.wq), wq_ref)
+    assert np.array_equal(f32bits(layer.w_scale), npbits(ws_ref))
+    assert np.array_equal(codes_np(layer.xq), xq_ref)
+    assert np.array_equal(f32bits(layer.x_scale), npbits(xs_ref))
+    assert O.bf16_ulp_distance(y_bits(y_host), y_ref).max() <= 1
+    # the device copy of Y is the one that was copied out
+    assert torch.equal(layer.y.cpu().view(torch.int16), y_host.view(torch.int16))
+
+
 # ------------------------------------------------------------------ static activation scale
 # Calibrate on X, then quantize a runtime batch whose tokens are scaled by
 # up to 1.6x (so some codes clip): scale, codes and clip count bit-exact.

@@ -77,6 +77,24 @@ def test_argument_validation_needs_no_device(lib):
     assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 4, 4, 24, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
     assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 0, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
     assert h.sq_w8a8_gemm(odd, aligned, aligned, aligned, 0, 4, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
+    # whole path from host memory: null host buffer, cin % 16, missing device buffer, workspace
+    full = {n: type("T", (), {"data_ptr": lambda self: 4096})() for n in
+            ("x", "w", "amax_x", "amax_w", "s", "s_inv", "wq", "w_scale", "xq", "x_scale", "y")}
+    ws = type("W", (), {"data_ptr": lambda self: 8192, "numel": lambda self: 1 << 20,
+                        "element_size": lambda self: 1})()
+    b = sq.linear_buffers(full, ws)
+    L = h.sq_linear_host
+    assert L(None, aligned, sq.SQ_BF16, 4, 32, 8, 0.5, 0, aligned, ctypes.byref(b), None, None) == sq.SQ_ERR_INVALID_ARG
+    assert L(aligned, aligned, sq.SQ_BF16, 4, 24, 8, 0.5, 0, aligned, ctypes.byref(b), None, None) == sq.SQ_ERR_INVALID_ARG
+    assert L(aligned, aligned, sq.SQ_BF16, 4, 32, 8, 1.5, 0, aligned, ctypes.byref(b), None, None) == sq.SQ_ERR_INVALID_ARG
+    b.xq = 4097
+    assert L(aligned, aligned, sq.SQ_BF16, 4, 32, 8, 0.5, 0, aligned, ctypes.byref(b), None, None) == sq.SQ_ERR_INVALID_ARG
+    b.xq = 4096
+    b.s = None
+    assert L(aligned, aligned, sq.SQ_BF16, 4, 32, 8, 0.5, 0, aligned, ctypes.byref(b), None, None) == sq.SQ_ERR_INVALID_ARG
+    b.s = 4096
+    b.ws_bytes = 0
+    assert L(aligned, aligned, sq.SQ_BF16, 4, 32, 8, 0.5, 0, aligned, ctypes.byref(b), None, None) == sq.SQ_ERR_WORKSPACE
 
 
 def test_kernel_counts_need_no_device(lib):

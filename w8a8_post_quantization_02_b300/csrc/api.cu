@@ -280,4 +280,53 @@ sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq, con
   return gemm_bf16c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, stream);
 }
 
+sq_status sq_linear_host(const void* x_host, const void* w_host, sq_dtype dt, int64_t tokens,
+                         int64_t cin, int64_t cout, float alpha, sq_codes fmt, void* y_host,
+                         const sq_linear_buffers* dev, int32_t* dev_flags, cudaStream_t stream) {
+  // every condition the steps check, before anything is enqueued
+  if (!x_host || !w_host || !y_host || !dev || !valid_dtype(dt) || !valid_codes(fmt) ||
+      tokens < 1 || cin < 1 || cout < 1 || cin % 16 != 0 || !(alpha >= 0.0f && alpha <= 1.0f))
+    return SQ_ERR_INVALID_ARG;
+  const sq_linear_buffers& b = *dev;
+  const void* const any[] = {b.x, b.w, b.amax_x, b.amax_w, b.s, b.s_inv, b.wq, b.w_scale, b.xq,
+                             b.x_scale, b.y};
+  for (const void* p : any)
+    if (!p) return SQ_ERR_INVALID_ARG;
+  const void* const words[] = {b.amax_x, b.amax_w, b.w_scale, b.x_scale, b.y};
+  for (const void* p : words)
+    if (reinterpret_cast<uintptr_t>(p) & 3) return SQ_ERR_INVALID_ARG;
+  if (!aligned16(b.x) || !aligned16(b.xq) || !aligned16(b.wq) || !aligned16(b.s_inv) ||
+      (reinterpret_cast<uintptr_t>(b.s) & 3) || (reinterpret_cast<uintptr_t>(b.w) % elem_bytes(dt)))
+    return SQ_ERR_INVALID_ARG;
+  if (cin > quant_act_max_cin(dt)) return SQ_ERR_UNSUPPORTED;
+  if (!b.workspace || b.ws_bytes < sq_workspace_bytes(SQ_OP_FOLD_QUANTIZE, 0, cout, cin, fmt) ||
+      (reinterpret_cast<uintptr_t>(b.workspace) & 3))
+    return SQ_ERR_WORKSPACE;
+
+  const size_t eb = (size_t)elem_bytes(dt);
+  if (cudaMemcpyAsync(b.x, x_host, (size_t)tokens * cin * eb, cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(b.w, w_host, (size_t)cin * cout * eb, cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess)
+    return SQ_ERR_CUDA;
+  sq_status r;
+  if ((r = sq_calibrate_absmax(b.x, dt, tokens, cin, cin, 0, 0, b.amax_x, stream)) != SQ_OK) return r;
+  if ((r = sq_calibrate_absmax(b.w, dt, cin, cout, cout, 1, 0, b.amax_w, stream)) != SQ_OK) return r;
+  if ((r = sq_smooth_factors(b.amax_x, b.amax_w, cin, alpha, b.s, b.s_inv, dev_flags, stream)) != SQ_OK)
+    return r;
+  if ((r = sq_fold_quantize_weight(b.w, dt, cin, cout, cout, b.s, b.wq, fmt, b.w_scale, dev_flags,
+                                   b.workspace, b.ws_bytes, stream)) != SQ_OK)
+    return r;
+  if ((r = sq_quant_act(b.x, dt, tokens, cin, cin, b.s_inv, b.xq, fmt, b.x_scale, dev_flags,
+                        stream)) != SQ_OK)
+    return r;
+  if ((r = sq_w8a8_gemm(b.xq, b.x_scale, b.wq, b.w_scale, fmt, tokens, cout, cin, b.y, nullptr,
+                        dev_flags, nullptr, 0, stream)) != SQ_OK)
+    return r;
+  if (cudaMemcpyAsync(y_host, b.y, (size_t)tokens * cout * 2, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return SQ_ERR_CUDA;
+  return SQ_OK;
+}
+
 }  // extern "C"

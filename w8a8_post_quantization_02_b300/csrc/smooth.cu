@@ -175,25 +175,34 @@ SQ_DEVINL float pow_rn32(float x, float y) {
 
 constexpr int kSmoothThreads = 64;
 
+// Two threads per channel: the even lane of each pair raises max|X_j| to
+// alpha, the odd lane max|W_j| to 1 - alpha, so the (double-precision)
+// powers of a block run on twice as many warps.
 __global__ void __launch_bounds__(kSmoothThreads) k_smooth(const float* __restrict__ amax_x,
                                                      const float* __restrict__ amax_w, int64_t cin,
                                                      float alpha, float* __restrict__ s,
                                                      float* __restrict__ s_inv, int32_t* flags) {
-  int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= cin) return;
-  float ax = amax_x[j], aw = amax_w[j];
-  if (!isfinite(ax) || !isfinite(aw)) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t j = t >> 1;
+  const bool odd = (t & 1) != 0;
+  const bool in = j < cin;
+  float ax = in ? amax_x[j] : 1.0f, aw = in ? amax_w[j] : 1.0f;
+  const bool finite = isfinite(ax) && isfinite(aw);
+  ax = fmaxf(ax, 1e-5f);
+  aw = fmaxf(aw, 1e-5f);
+  const float beta = __fsub_rn(1.0f, alpha);
+  // one call with per-lane operands (not two branches), so the pair does
+  // not diverge
+  const float mine = finite ? pow_rn32(odd ? aw : ax, odd ? beta : alpha) : 1.0f;
+  const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);  // every lane reaches this
+  if (!in || odd) return;
+  if (!finite) {
     s[j] = 1.0f;
     s_inv[j] = 1.0f;
     raise_flag(flags, SQ_FLAG_NONFINITE);
     return;
   }
-  ax = fmaxf(ax, 1e-5f);
-  aw = fmaxf(aw, 1e-5f);
-  const float beta = __fsub_rn(1.0f, alpha);
-  float p = pow_rn32(ax, alpha);
-  float q = pow_rn32(aw, beta);
-  float sj = __fdiv_rn(p, q);
+  float sj = __fdiv_rn(mine, other);
   sj = fminf(fmaxf(sj, 1e-5f), 1e5f);
   s[j] = sj;
   s_inv[j] = __fdiv_rn(1.0f, sj);
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kSmoothThreads) k_smooth(const float* __restri
 
 sq_status smooth_factors(const float* amax_x, const float* amax_w, int64_t cin, float alpha,
                          float* s, float* s_inv, int32_t* flags, cudaStream_t st) {
-  const int64_t g = (cin + kSmoothThreads - 1) / kSmoothThreads;
+  const int64_t g = (2 * cin + kSmoothThreads - 1) / kSmoothThreads;
   k_smooth<<<(unsigned)g, kSmoothThreads, 0, st>>>(amax_x, amax_w, cin, alpha, s, s_inv, flags);
   return launch_status();
 }

@@ -179,6 +179,20 @@ class Layer:
         counts = self.kernel_counts()
         return sum(counts[name] for name, _, _ in self.stages())
 
+    def linear_buffers(self) -> "sq.LinearBuffers":
+        """This layer's device buffers as the C ABI's sq_linear_buffers."""
+        names = ("x", "w", "amax_x", "amax_w", "s", "s_inv", "wq", "w_scale", "xq", "x_scale", "y")
+        return sq.linear_buffers({n: getattr(self, n) for n in names}, self.ws_fold)
+
+    def run_host(self, x_host: torch.Tensor, w_host: torch.Tensor, y_host: torch.Tensor,
+                 stream=None, bufs: "sq.LinearBuffers | None" = None) -> None:
+        """One step from host memory through the C ABI's sq_linear_host: X and
+        W copied in, the whole path (dynamic per-token scale), Y copied out."""
+        if self.act_scale != "dynamic":
+            raise ValueError("sq_linear_host runs the dynamic per-token activation scale")
+        sq.linear_host(x_host, w_host, self.alpha, self.codes, y_host,
+                       bufs if bufs is not None else self.linear_buffers(), self.flags, stream)
+
     def _enqueue(self, fns: dict, main, side) -> None:
         """Enqueue steps 1-4 on two streams.  The X side (absmax of X, then
         the activation codes) runs on ``side`` beside the W side (absmax of W,

@@ -25,6 +25,14 @@ SQ_CODES_I8, SQ_CODES_BF16 = 0, 1
 
 # name -> (restype, argtypes), mirroring include/sq.h
 _P, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class LinearBuffers(ctypes.Structure):
+    """sq_linear_buffers: the caller's device buffers for sq_linear_host."""
+    _fields_ = [(name, _P) for name in ("x", "w", "amax_x", "amax_w", "s", "s_inv", "wq", "w_scale",
+                                        "xq", "x_scale", "y", "workspace")] + [("ws_bytes", _SZ)]
+
+
 SIGNATURES = {
     "sq_calibrate_absmax": (_I32, [_P, _I32, _I64, _I64, _I64, _I32, _I32, _P, _P]),
     "sq_smooth_factors": (_I32, [_P, _P, _I64, _F, _P, _P, _P, _P]),
@@ -45,6 +53,8 @@ SIGNATURES = {
     "sq_weight_quant_error": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     "sq_layer_error": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _I64, _I64, _P, _P, _I32, _P, _P]),
     "sq_channel_stats": (_I32, [_P, _P, _I64, _P, _P]),
+    "sq_linear_host": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _F, _I32, _P, ctypes.POINTER(LinearBuffers),
+                              _P, _P]),
     "sq_status_string": (ctypes.c_char_p, [_I32]),
     "sq_check_device": (_I32, [_I32]),
 }
@@ -363,3 +373,31 @@ def smoothquant_linear(x: torch.Tensor, w: torch.Tensor, alpha: float, codes: st
     y, acc = r if want_acc else (r, None)
     return dict(amax_x=amax_x, amax_w=amax_w, s=s, s_inv=s_inv, wq=wq, w_scale=w_scale, xq=xq,
                 x_scale=x_scale, y=y, acc=acc)
+
+
+def linear_buffers(bufs: dict, workspace: torch.Tensor) -> LinearBuffers:
+    """Pack device tensors (keys as in sq_linear_buffers) for sq_linear_host."""
+    b = LinearBuffers()
+    for name, _ in LinearBuffers._fields_[:-2]:
+        setattr(b, name, bufs[name].data_ptr())
+    b.workspace = workspace.data_ptr()
+    b.ws_bytes = workspace.numel() * workspace.element_size()
+    return b
+
+
+def linear_host(x_host: torch.Tensor, w_host: torch.Tensor, alpha: float, codes: str,
+                y_host: torch.Tensor, dev: LinearBuffers, flags: torch.Tensor | None = None,
+                stream=None) -> None:
+    """The whole path on host tensors (pinned for asynchronous copies):
+    X and W copied in, steps 1-5 on the device buffers `dev`, Y copied out
+    into y_host, all enqueued on `stream`."""
+    for t, name in ((x_host, "x_host"), (w_host, "w_host"), (y_host, "y_host")):
+        if t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D host tensor")
+    if y_host.dtype != torch.bfloat16:
+        raise ValueError("y_host must be bfloat16")
+    tokens, cin = x_host.shape
+    cout = w_host.shape[1]
+    _check("sq_linear_host", load_library().sq_linear_host(
+        _ptr(x_host), _ptr(w_host), _dtype_code(x_host), tokens, cin, cout, alpha, _codes_fmt(codes),
+        _ptr(y_host), ctypes.byref(dev), _ptr(flags), _stream(stream)))
