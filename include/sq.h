@@ -9,6 +9,8 @@
  *   4. sq_quant_act             X' = X diag(s)^-1, per-token INT8 codes
  *   5. sq_w8a8_gemm             exact INT8 x INT8 accumulation, bf16 epilogue
  *
+ * sq_linear_host runs all five on inputs in host memory (copies included).
+ *
  * Orientation (first source page, "Move activation scale without changing
  * the real linear map", paragraph 1): X is [tokens x Cin] and W is
  * [Cin x Cout], so Y = X W; diag(s) multiplies W on its rows (input

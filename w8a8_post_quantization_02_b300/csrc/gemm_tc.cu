@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < C::COLS; ++i) acc[i] = 0;
       for (int c = 0; c < P.n_chunks; ++c) {
         const uint32_t buf = chunk_ctr & 1, use = chunk_ctr >> 1;
-        // one lane waits and the warp follows its verdict, so the warp stays
+        // one lane waits and the warp follows its result, so the warp stays
         // converged for the .sync.aligned TMEM loads
         int got = 1;
         if (lane == 0) got = mbar_wait(&sm.acc_full[buf], use & 1, &sm.abort, flags) ? 1 : 0;
