@@ -624,7 +624,7 @@ def test_rmsnorm_nonfinite_flag(sq):
 
 
 # ------------------------------------------------------------------ Smooth Rotation
-ROT_ACT_SHAPES = [(64, 512, "f32"), (37, 256, "bf16"), (300, 4096, "bf16"), (9, 8192, "f32"),
+ROT_ACT_SHAPES = [(64, 512, "f32"), (37, 256, "bf16"), (5, 512, "bf16"), (300, 4096, "bf16"), (9, 8192, "f32"),
                   (129, 16384, "bf16"), (40, 32768, "bf16"), (77, 11008, "bf16")]
 
 

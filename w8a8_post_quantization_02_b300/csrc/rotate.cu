@@ -249,14 +249,19 @@ sq_status rows_dispatch(const uint8_t* x, int64_t rows, int64_t len, int64_t ld_
   constexpr int E = BF16 ? 8 : 4;
   const int nvec = (int)(len / E);
   const int log2_len = pow2_shift;
-  // the fewest threads (>= 32) holding the row in 1, 2 or 4 vectors each
+  // without the rotation: the fewest threads (>= 32) holding the row in 1,
+  // 2 or 4 vectors each
   int vpt = 1;
   while (vpt < 4 && (nvec + vpt - 1) / vpt > 1024) vpt *= 2;
   int nt = (nvec + vpt - 1) / vpt;
   if (nt > 1024) return SQ_ERR_UNSUPPORTED;
   nt = (nt + 31) / 32 * 32;
-  if (rotate && nt * vpt != nvec) {
-    // a power-of-two row: whole warps of whole vectors
+  if (rotate) {
+    // a power-of-two row, whole warps of whole vectors, as many vectors per
+    // thread as allowed (4): every factor of 2 in the vectors per thread
+    // moves one transform stage from shared memory (two block barriers)
+    // into registers, and smaller blocks let more rows share an SM
+    vpt = 4;
     while (vpt > 1 && nvec / vpt < 32) vpt /= 2;
     nt = nvec / vpt;
     if (nt < 32 || nt > 1024 || nt * vpt != nvec) return SQ_ERR_UNSUPPORTED;
