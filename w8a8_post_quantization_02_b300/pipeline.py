@@ -190,6 +190,10 @@ class Layer:
         W copied in, the whole path (dynamic per-token scale), Y copied out."""
         if self.act_scale != "dynamic":
             raise ValueError("sq_linear_host runs the dynamic per-token activation scale")
+        # the device buffers are this layer's: the host tensors must match them
+        if (tuple(x_host.shape) != tuple(self.x.shape) or tuple(w_host.shape) != tuple(self.w.shape)
+                or x_host.dtype != self.x.dtype or w_host.dtype != self.w.dtype):
+            raise ValueError("x_host / w_host do not match this layer's shapes and dtype")
         sq.linear_host(x_host, w_host, self.alpha, self.codes, y_host,
                        bufs if bufs is not None else self.linear_buffers(), self.flags, stream)
 

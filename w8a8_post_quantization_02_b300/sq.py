@@ -396,8 +396,13 @@ def linear_host(x_host: torch.Tensor, w_host: torch.Tensor, alpha: float, codes:
             raise ValueError(f"{name} must be a contiguous 2-D host tensor")
     if y_host.dtype != torch.bfloat16:
         raise ValueError("y_host must be bfloat16")
+    if w_host.dtype != x_host.dtype:
+        raise ValueError("x_host and w_host must have the same dtype")
     tokens, cin = x_host.shape
     cout = w_host.shape[1]
+    if w_host.shape[0] != cin or tuple(y_host.shape) != (tokens, cout):
+        raise ValueError(f"shapes do not chain: x {tuple(x_host.shape)}, w {tuple(w_host.shape)}, "
+                         f"y {tuple(y_host.shape)}")
     _check("sq_linear_host", load_library().sq_linear_host(
         _ptr(x_host), _ptr(w_host), _dtype_code(x_host), tokens, cin, cout, alpha, _codes_fmt(codes),
         _ptr(y_host), ctypes.byref(dev), _ptr(flags), _stream(stream)))
