@@ -109,3 +109,17 @@ def test_kernel_counts_need_no_device(lib):
     for op in (sq.SQ_OP_SMOOTH, sq.SQ_OP_QUANT_ACT, sq.SQ_OP_GEMM):
         assert h.sq_kernel_count(op, sq.SQ_BF16, 2048, 11008, 4096, 4096, 0, 0) == 1
     assert h.sq_kernel_count(99, sq.SQ_BF16, 1, 1, 16, 16, 0, 0) == -1
+
+
+def test_host_binding_checks_shapes_and_dtypes(lib):
+    import torch
+    from w8a8_post_quantization_02_b300 import sq
+    b = sq.LinearBuffers()
+    x = torch.zeros(4, 32, dtype=torch.bfloat16)
+    y = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # W's dtype differs from X's
+        sq.linear_host(x, torch.zeros(32, 8, dtype=torch.float32), 0.5, "i8", y, b)
+    with pytest.raises(ValueError):  # X's columns and W's rows do not chain
+        sq.linear_host(x, torch.zeros(16, 8, dtype=torch.bfloat16), 0.5, "i8", y, b)
+    with pytest.raises(ValueError):  # Y is not tokens x cout
+        sq.linear_host(x, torch.zeros(32, 8, dtype=torch.bfloat16), 0.5, "i8", torch.zeros(4, 9, dtype=torch.bfloat16), b)
