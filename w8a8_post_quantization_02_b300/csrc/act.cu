@@ -487,13 +487,11 @@ sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_byt
                      const float* s_inv, uint8_t* xq, float* x_scale, int32_t* flags, Static sc,
                      cudaStream_t st) {
   auto kern = k_quant_act<BF16, CODES, NT, VPT, MODE>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-        cudaSuccess)
-      return SQ_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (!once_per_device(attr_done, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      }))
+    return SQ_ERR_CUDA;
   const size_t row_bytes = (size_t)nvec * 16;
   // about 32 KiB of rows in flight per CTA, at least two stages, so several
   // CTAs share an SM.  Measured on B300 against 64 KiB: 2048 x 4096 bf16

@@ -336,12 +336,11 @@ sq_status launch(const CUtensorMap& map, int64_t rows, int64_t cols, int rpc, in
                  uint32_t* out, cudaStream_t st) {
   auto kern = k_colmax_strip<BF16, CL>;
   const size_t smem = sizeof(Smem) + 1024;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return SQ_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (!once_per_device(attr_done, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      }))
+    return SQ_ERR_CUDA;
   const int64_t strips = (cols * (BF16 ? 2 : 4) + kRowBytes - 1) / kRowBytes;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(strips * CL), 1, 1);

@@ -509,12 +509,11 @@ sq_status launch(const void* xq, const float* x_scale, const void* wq, const flo
   if (!make_map(&ma, xq, m, k, BM) || !make_map(&mb, wq, n, k, C::B_ROWS)) return SQ_ERR_CUDA;
   auto kern = k_gemm_bf16c<CG, BN>;
   const size_t smem = sizeof(Smem<CG, BN>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return SQ_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (!once_per_device(attr_done, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      }))
+    return SQ_ERR_CUDA;
   Problem P;
   P.M = m;
   P.N = n;

@@ -226,12 +226,11 @@ sq_status launch_rows(const uint8_t* x, int64_t rows, int nvec, int64_t ld_bytes
                       float* row_scale, int32_t* flags, cudaStream_t st) {
   auto kern = k_rotate_rows<BF16, CODES, VPT, ROTATE>;
   const size_t smem = (ROTATE ? (size_t)nvec * (BF16 ? 8 : 4) * 4 : 0) + 32 * 4;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
-      return SQ_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (!once_per_device(attr_done, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      }))
+    return SQ_ERR_CUDA;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt, smem) != cudaSuccess) return SQ_ERR_CUDA;
   occ = std::max(1, std::min(occ, 8));

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "sq.h"
 
@@ -22,18 +23,37 @@ inline sq_status launch_status() {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Kernel attributes (shared-memory limits) are per device: `set` runs once
+// for each device the calling thread has current (device ids below 64 are
+// remembered in `done`; others run it every time).  Safe to call from
+// several host threads: `set` is idempotent.  False if `set` failed.
+template <typename F>
+inline bool once_per_device(std::atomic<uint64_t>& done, F set) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+  if (set() != cudaSuccess) return false;
+  done.fetch_or(bit, std::memory_order_release);
+  return true;
+}
+
 inline int elem_bytes(sq_dtype dt) { return dt == SQ_F32 ? 4 : 2; }
 
 inline int code_bytes(sq_codes f) { return f == SQ_CODES_BF16 ? 2 : 1; }
 
+// SM count of the current device, queried once per device (ids below 64).
 inline int sm_count() {
-  static int n = 0;  // queried once; the device does not change its SM count
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static std::atomic<int> cache[64];  // zero-initialized: static storage
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

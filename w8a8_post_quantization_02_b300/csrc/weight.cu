@@ -445,14 +445,14 @@ sq_status launch(const CUtensorMap& map, const float* s, int64_t cin, int64_t co
   constexpr int EPC = BF16 ? 8 : 4;
   auto kern = k_fold_strip<BF16, CODES, CL>;
   const size_t smem = Layout<EPC>(rpc).total + 1024;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<EPC>(kMaxRows).total + 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-      return SQ_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (!once_per_device(attr_done, [&] {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)Layout<EPC>(kMaxRows).total + 1024);
+        return e != cudaSuccess ? e
+                                : cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      }))
+    return SQ_ERR_CUDA;
   const int64_t strips = (cout + 4 * EPC - 1) / (4 * EPC);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(strips * CL), 1, 1);
