@@ -236,6 +236,8 @@ def to_device(case, torch):
 NCU_TRAFFIC_BYTES = {
     # 109.38 MB read + 26.36 MB written (the rest of Y still dirty in L2)
     ("k_gemm_bf16c", "prefill_upgate_2048x4096x11008"): 135.74e6,
+    # 16.88 MB read (the int8 weight codes and X codes), nothing written back yet
+    ("k_gemm_i8_mma", "decode_7b_16x4096x4096"): 16.88e6,
 }
 
 
