@@ -37,10 +37,11 @@ Readings where the pages are silent:
 3. the runtime scaling multiplies by S^-1, i.e. X'[t,j] = X[t,j] * (1/s_j)
    with 1/s_j one binary32 division; the fold multiplies W's rows (input
    channels) by s_j.
-4. symmetric INT8 quantizer with scale d = amax / 127 (binary32 division;
-   d = 1 when amax == 0) and codes clamp(rne(v * (1/d)), -127, 127), the
-   reciprocal 1/d one binary32 division; per output channel for W, per
-   token (dynamic) for X.
+4. symmetric INT8 quantizer (the review's ``core_discovery``: symmetric
+   round-to-nearest) with scale d = amax / 127 (binary32 division; d = 1
+   when amax == 0) and codes clamp(rne(v / d), -127, 127), v / d one
+   binary32 division (the plain definition of round(v / step)); per output
+   channel for W, per token (dynamic) for X.
 5. the GEMM accumulates exactly (int64 here) and its epilogue rounds
    acc * x_scale * w_scale, evaluated in float64, once to bf16 (RNE).
 """
@@ -138,22 +139,30 @@ def smooth_factors(amax_x, amax_w, alpha):
 # --------------------------------------------------------------------------
 # shared quantizer definition (reading 4)
 # --------------------------------------------------------------------------
-def _scale_and_inverse(amax: np.ndarray):
+def _scale(amax: np.ndarray):
+    """d = amax / 127 (one binary32 division), 1 where amax == 0; and
+    whether any amax is non-finite."""
     amax = np.asarray(amax, dtype=F32)
     nonfinite = bool((~np.isfinite(amax)).any())
     with np.errstate(invalid="ignore", over="ignore"):
         d = (amax / F32(QMAX)).astype(F32)
         d = np.where(amax == 0, F32(1.0), d).astype(F32)
-        inv = (F32(1.0) / d).astype(F32)
-    return d, inv, nonfinite
+    return d, nonfinite
 
 
-def _codes(v: np.ndarray, inv: np.ndarray) -> np.ndarray:
+def _quotients(v: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """v / d, one IEEE binary32 division per element."""
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        return (np.asarray(v, F32) / np.asarray(d, F32)).astype(F32)
+
+
+def _codes(v: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """clamp(rne(v / d), -127, 127); a NaN quotient gives code 0."""
+    t = _quotients(v, d)
     with np.errstate(invalid="ignore", over="ignore"):
-        t = (v * inv).astype(F32)  # one binary32 multiply
         r = np.rint(t)             # round half to even
         r = np.clip(r, -QMAX, QMAX)
-        r = np.where(np.isfinite(r), r, 0)
+        r = np.where(np.isnan(r), 0, r)
     return r.astype(np.int8)
 
 
@@ -175,8 +184,8 @@ def fold_quantize_weight(w, s, return_folded: bool = False):
     with np.errstate(over="ignore", invalid="ignore"):
         wf = (s32[:, None] * w32).astype(F32)
     amax = np.max(np.abs(wf), axis=0).astype(F32)
-    d, inv, nonfinite = _scale_and_inverse(amax)
-    q = _codes(wf, inv[None, :])
+    d, nonfinite = _scale(amax)
+    q = _codes(wf, d[None, :])
     wq = np.ascontiguousarray(q.T)
     if return_folded:
         return wq, d, nonfinite, wf
@@ -199,8 +208,8 @@ def quant_act(x, s_inv, return_scaled: bool = False):
     with np.errstate(over="ignore", invalid="ignore"):
         xs = (x32 * si[None, :]).astype(F32)
     amax = np.max(np.abs(xs), axis=1).astype(F32) if xs.shape[1] else np.zeros(xs.shape[0], F32)
-    d, inv, nonfinite = _scale_and_inverse(amax)
-    q = _codes(xs, inv[:, None])
+    d, nonfinite = _scale(amax)
+    q = _codes(xs, d[:, None])
     if return_scaled:
         return q, d, nonfinite, xs
     return q, d, nonfinite
@@ -227,7 +236,7 @@ def static_act_scale(amax_x, s_inv):
     m = F32(np.max(v)) if v.size else F32(0)
     if np.isnan(v).any():
         m = F32(np.nan)
-    d, _, nonfinite = _scale_and_inverse(np.array([m], dtype=F32))
+    d, nonfinite = _scale(np.array([m], dtype=F32))
     return F32(d[0]), nonfinite
 
 
@@ -235,22 +244,22 @@ def quant_act_static(x, s_inv, d):
     """X' = X * (1/s), codes with one fixed scale d for every token.
 
     Same quantizer as ``quant_act`` (reading 4) with the per-token scale
-    replaced by the calibrated d: codes clamp(rne(X' * (1/d)), -127, 127).
+    replaced by the calibrated d: codes clamp(rne(X' / d), -127, 127).
     Runtime activations may exceed the calibration maximum, so the clamp
-    can act; ``clipped`` counts the elements it changed.  Returns ``(xq,
-    x_scale, clipped)`` with x_scale = d for every token, so the GEMM's
-    epilogue is unchanged.
+    can act; ``clipped`` counts the elements it changed (a quotient that
+    overflows to infinity, like a non-finite X', saturates uncounted).
+    Returns ``(xq, x_scale, clipped)`` with x_scale = d for every token, so
+    the GEMM's epilogue is unchanged.
     """
     x32 = np.asarray(x, dtype=F32)
     si = np.asarray(s_inv, dtype=F32)
     d = F32(d)
-    inv = F32(F32(1.0) / d)
     with np.errstate(over="ignore", invalid="ignore"):
         xs = (x32 * si[None, :]).astype(F32)
-        t = (xs * inv).astype(F32)
-        r = np.rint(t)
+    t = _quotients(xs, np.full((xs.shape[0], 1), d, dtype=F32))
+    r = np.rint(t)
     clipped = int(np.count_nonzero(np.isfinite(r) & (np.abs(r) > QMAX)))
-    q = _codes(xs, np.full(xs.shape[0], inv, dtype=F32)[:, None])
+    q = _codes(xs, np.full((xs.shape[0], 1), d, dtype=F32))
     return q, np.full(xs.shape[0], d, dtype=F32), clipped
 
 
@@ -331,8 +340,8 @@ def rmsnorm_quant_act(h, gamma_folded, eps, return_scaled=False):
     with np.errstate(over="ignore", invalid="ignore"):
         xs = ((h32 * r[:, None]).astype(F32) * np.asarray(gamma_folded, F32)[None, :]).astype(F32)
     amax = np.max(np.abs(xs), axis=1).astype(F32) if xs.shape[1] else np.zeros(xs.shape[0], F32)
-    d, inv, nonfinite = _scale_and_inverse(amax)
-    q = _codes(xs, inv[:, None])
+    d, nonfinite = _scale(amax)
+    q = _codes(xs, d[:, None])
     if return_scaled:
         return q, d, nonfinite, xs
     return q, d, nonfinite
@@ -493,10 +502,10 @@ def _rows_quantized(z, qmax):
     with np.errstate(invalid="ignore", over="ignore"):
         d = (amax / F32(qmax)).astype(F32)
         d = np.where(amax == 0, F32(1.0), d).astype(F32)
-        inv = (F32(1.0) / d).astype(F32)
-        t = (z * inv[:, None]).astype(F32)
+    t = _quotients(z, d[:, None])
+    with np.errstate(invalid="ignore", over="ignore"):
         r = np.clip(np.rint(t), -qmax, qmax)
-        r = np.where(np.isfinite(r), r, 0)
+        r = np.where(np.isnan(r), 0, r)
     return r.astype(np.int8), d, nonfinite
 
 

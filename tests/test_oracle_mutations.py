@@ -25,6 +25,7 @@ def _pins():
         P.test_lone_outlier_becomes_geometric_mean,
         P.test_calibrate_matches_loops,
         P.test_rne_ties_and_clamp,
+        P.test_codes_divide_by_the_scale,
         P.test_absmax_element_maps_to_127,
         P.test_zero_rows_and_columns,
         P.test_nonfinite_statistics_flagged,
@@ -69,8 +70,8 @@ def fold_scales_columns(w, s, return_folded=False):
     wf = w32.copy()
     wf[:, :k] = (w32[:, :k] * s32[None, :k]).astype(F32)   # columns, not rows
     amax = np.max(np.abs(wf), axis=0).astype(F32)
-    d, inv, nf = O._scale_and_inverse(amax)
-    q = O._codes(wf, inv[None, :])
+    d, nf = O._scale(amax)
+    q = O._codes(wf, d[None, :])
     wq = np.ascontiguousarray(q.T)
     return (wq, d, nf, wf) if return_folded else (wq, d, nf)
 
@@ -83,18 +84,18 @@ def calibrate_wrong_axis(a, axis, prev=None):
     return ORIG["calibrate_absmax"](a, 1 - axis, prev)
 
 
-def codes_round_half_up(v, inv):
+def codes_round_half_up(v, d):
+    t = O._quotients(v, d)
     with np.errstate(invalid="ignore", over="ignore"):
-        t = (v * inv).astype(F32)
         r = np.floor(t + F32(0.5))
         r = np.clip(r, -O.QMAX, O.QMAX)
         r = np.where(np.isfinite(r), r, 0)
     return r.astype(np.int8)
 
 
-def codes_clamp_128(v, inv):
+def codes_clamp_128(v, d):
+    t = O._quotients(v, d)
     with np.errstate(invalid="ignore", over="ignore"):
-        t = (v * inv).astype(F32)
         r = np.clip(np.rint(t), -128, 127)
         r = np.where(np.isfinite(r), r, 0)
     return r.astype(np.int8)
@@ -104,16 +105,21 @@ def scale_divides_by_128(amax):
     amax = np.asarray(amax, F32)
     with np.errstate(invalid="ignore", over="ignore"):
         d = np.where(amax == 0, F32(1.0), (amax / F32(128))).astype(F32)
-        inv = (F32(1.0) / d).astype(F32)
-    return d, inv, bool((~np.isfinite(amax)).any())
+    return d, bool((~np.isfinite(amax)).any())
+
+
+def quotients_by_reciprocal(v, d):
+    inv = (F32(1.0) / np.asarray(d, F32)).astype(F32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        return (np.asarray(v, F32) * inv).astype(F32)             # v * RN(1/d), not RN(v/d)
 
 
 def act_scale_per_channel(x, s_inv, return_scaled=False):
     x32, si = np.asarray(x, F32), np.asarray(s_inv, F32)
     xs = (x32 * si[None, :]).astype(F32)
     amax = np.max(np.abs(xs), axis=0).astype(F32)           # over tokens, not channels
-    d, inv, nf = O._scale_and_inverse(amax)
-    q = O._codes(xs, inv[None, :])
+    d, nf = O._scale(amax)
+    q = O._codes(xs, d[None, :])
     tok = np.full(xs.shape[0], d.max(initial=F32(1.0)), F32)
     return (q, tok, nf, xs) if return_scaled else (q, tok, nf)
 
@@ -191,7 +197,7 @@ def rows_quantized_qmax_plus_one(z, qmax):
 
 
 ORIG = {name: getattr(O, name) for name in (
-    "fold_quantize_weight", "smooth_factors", "calibrate_absmax", "_codes", "_scale_and_inverse",
+    "fold_quantize_weight", "smooth_factors", "calibrate_absmax", "_codes", "_scale", "_quotients",
     "quant_act", "w8a8_gemm", "static_act_scale", "act_quant_error", "weight_quant_error",
     "channel_stats", "_rows_quantized")}
 
@@ -201,7 +207,8 @@ MUTATIONS = {
     "calibration reduces the other axis": ("calibrate_absmax", calibrate_wrong_axis),
     "codes round half up": ("_codes", codes_round_half_up),
     "codes clamp to [-128, 127]": ("_codes", codes_clamp_128),
-    "scale = amax / 128": ("_scale_and_inverse", scale_divides_by_128),
+    "scale = amax / 128": ("_scale", scale_divides_by_128),
+    "codes multiply by a rounded reciprocal": ("_quotients", quotients_by_reciprocal),
     "activation scale per channel": ("quant_act", act_scale_per_channel),
     "epilogue drops w_scale": ("w8a8_gemm", epilogue_drops_w_scale),
     "s_inv not inverted": ("smooth_factors", s_inv_not_inverted),

@@ -88,8 +88,7 @@ def brute_path(x, w, alpha_kind):
     def quant(vals):
         amax = max(abs(v) for v in vals)
         d = Fr(1) if amax == 0 else rn32(amax / 127)
-        inv = rn32(1 / d)
-        codes = [max(-127, min(127, round(rn32(v * inv)))) for v in vals]
+        codes = [max(-127, min(127, round(rn32(v / d)))) for v in vals]
         return codes, d
 
     wf = [[rn32(s[j] * W[j][n]) for n in range(N)] for j in range(K)]
@@ -239,6 +238,58 @@ def test_rne_ties_and_clamp():
     q, d, nf = O.quant_act(x, np.ones(x.shape[1], F32))
     assert d.tolist() == [1.0] and not nf
     assert q.tolist() == [[2, 4, -2, 0, 2, -127, 127, 126, 0]]
+
+
+def division_split_cases(qmax, count, seed):
+    """Pairs (amax, v) with |v| < amax where the code of v under the scale
+    d = RN(amax / qmax), rne(RN(v / d)), differs from the code a reciprocal
+    would give, rne(RN(v * RN(1 / d))).  Found and decided in exact rational
+    arithmetic (no binary32 division is used), next to half-integer
+    multiples of d, where the two roundings can part."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        amax = F32(rng.uniform(0.5, 100.0))
+        d = rn32(Fr(float(amax)) / qmax)
+        inv = rn32(1 / d)
+        k = int(rng.integers(0, qmax)) + Fr(1, 2)
+        v0 = F32(float(k * d))
+        for step in range(-3, 4):
+            v = v0
+            for _ in range(abs(step)):
+                v = np.nextafter(v, F32(np.inf) if step > 0 else F32(-np.inf))
+            if not abs(v) < amax:
+                continue
+            by_div = round(rn32(Fr(float(v)) / d))
+            by_rcp = round(rn32(Fr(float(v)) * inv))
+            if by_div != by_rcp:
+                sign = -1 if len(out) % 2 else 1
+                out.append((amax, F32(sign * v), sign * by_div, sign * by_rcp))
+                break
+    return out
+
+
+def test_codes_divide_by_the_scale():
+    """The quantizer's code is rne(v / d) with v / d one IEEE binary32
+    division (the review's core_discovery: symmetric round-to-nearest, i.e.
+    round(v / step)), not v times a rounded reciprocal: crafted elements
+    whose two codes differ take the division's, for the per-token
+    activation quantizer, the per-channel weight quantizer, the static
+    scale and the low-bit rows of the rotated quantizer."""
+    cases = division_split_cases(127, 8, seed=11)
+    for amax, v, want, other in cases:
+        assert want != other
+        x = np.array([[amax, v]], F32)
+        q, d, _ = O.quant_act(x, np.ones(2, F32))
+        assert Fr(float(d[0])) == rn32(Fr(float(amax)) / 127)
+        assert q.tolist() == [[127, want]]
+        wq, _, _ = O.fold_quantize_weight(x.T.copy(), np.ones(2, F32))
+        assert wq.tolist() == [[127, want]]
+        qs, _, clipped = O.quant_act_static(x, np.ones(2, F32), d[0])
+        assert qs.tolist() == [[127, want]] and clipped == 0
+    for amax, v, want, other in division_split_cases(7, 6, seed=12):
+        q, _, _ = O.rotate_quant_act(np.array([[amax, v]], F32), None, False, 7)
+        assert q.tolist() == [[7, want]]
 
 
 def test_absmax_element_maps_to_127():
