@@ -28,7 +28,12 @@
  *     nothing is enqueued.  A failed launch returns SQ_ERR_CUDA.
  *   - Data-dependent conditions found on the device are OR-ed into the
  *     optional device word `dev_flags` (SQ_FLAG_*), which the caller zeroes
- *     and reads back when it wants them.  Kernels never trap.
+ *     and reads back when it wants them; sq_read_device_flags turns the
+ *     word into a status (SQ_ERR_TIMEOUT, SQ_ERR_NONFINITE).  The word is
+ *     the caller's, one per stream or per layer as it likes, rather than
+ *     an error word inside the library: the library keeps no mutable state,
+ *     so concurrent streams and captured graphs never share a status.
+ *     Kernels never trap.
  *   - Row-major matrices take a leading dimension `ld` in elements.  The
  *     kernels move 16-byte vectors: code buffers, and X in step 4, must be
  *     16-byte aligned with rows a multiple of 16 bytes.  The inputs of steps
@@ -51,10 +56,11 @@ extern "C" {
 typedef enum {
   SQ_OK = 0,
   SQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, alignment or enum */
-  SQ_ERR_NONFINITE = 2,    /* reserved for host-side checks of host data */
+  SQ_ERR_NONFINITE = 2,    /* the device word reports a NaN/Inf statistic or scale */
   SQ_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
   SQ_ERR_UNSUPPORTED = 4,  /* valid request this build does not implement */
-  SQ_ERR_WORKSPACE = 5     /* workspace pointer missing or too small */
+  SQ_ERR_WORKSPACE = 5,    /* workspace pointer missing or too small */
+  SQ_ERR_TIMEOUT = 6       /* the device word reports a bounded wait that ran out */
 } sq_status;
 
 /* Bits OR-ed into *dev_flags by the kernels. */
@@ -135,7 +141,9 @@ sq_status sq_smooth_factors(const float* amax_x, const float* amax_w, int64_t ci
  * INT8).  For output channel n:
  *   W'[j,n] = s[j] * W[j,n]               (fp32 multiply)
  *   w_scale[n] = max_j |W'[j,n]| / 127    (fp32 division; 1 if the max is 0)
- *   wq[n,j] = clamp(rne(W'[j,n] * (1 / w_scale[n])), -127, 127)
+ *   wq[n,j] = clamp(rne(W'[j,n] / w_scale[n]), -127, 127)
+ * where W'/w_scale is the IEEE fp32 quotient (Smooth Rotation review,
+ * core_discovery: symmetric round-to-nearest, i.e. round(v / step)).
  *   w      device [cin x cout] row-major, type dt, leading dim ldw
  *   s      device fp32 [cin]
  *   wq     device [cout x cin] codes, row n contiguous (K-major), format fmt
@@ -161,9 +169,11 @@ sq_status sq_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin, int64
  * array of SQ_NOALLOC_MAX_COUT entries (256 KiB) in the library's device
  * memory, which every GPU that loads the library holds until exit.
  *   - cout > SQ_NOALLOC_MAX_COUT -> SQ_ERR_WORKSPACE (nothing enqueued).
- *   - The first call on each device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ *   - Each call looks up the array's device address on the current device
+ *     (so a device reset, which moves the array, is harmless); a call made
+ *     during stream capture reuses the address the last call on that
+ *     device found, so make the first call on each device before any
+ *     stream capture.
  *   - All calls share the one array: calls whose work overlaps on the GPU
  *     (e.g. on two streams) race and give wrong results.  Each call clears
  *     the entries it uses before using them.
@@ -182,7 +192,7 @@ sq_status sq_fold_quantize_weight_noalloc(const void* w, sq_dtype dt, int64_t ci
  * For token t:
  *   X'[t,j] = X[t,j] * s_inv[j]           (fp32 multiply)
  *   x_scale[t] = max_j |X'[t,j]| / 127    (fp32 division; 1 if the max is 0)
- *   xq[t,j] = clamp(rne(X'[t,j] * (1 / x_scale[t])), -127, 127)
+ *   xq[t,j] = clamp(rne(X'[t,j] / x_scale[t]), -127, 127)   (fp32 quotient)
  *   x      device [tokens x cin] row-major, type dt, leading dim ldx
  *   s_inv  device fp32 [cin] (from step 2)
  *   xq     device [tokens x cin] codes, row-major, format fmt
@@ -209,7 +219,7 @@ sq_status sq_quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, 
  *   dev_flags      device int32 or NULL (SQ_FLAG_NONFINITE)
  *
  * sq_quant_act_static: X' = X * s_inv, codes with the one scale d:
- *   xq[t,j] = clamp(rne(X'[t,j] * (1/d)), -127, 127);  x_scale[t] = d
+ *   xq[t,j] = clamp(rne(X'[t,j] / d), -127, 127);  x_scale[t] = d
  * (x_scale is filled so that sq_w8a8_gemm's epilogue is unchanged).  Values
  * beyond the calibration maximum saturate; `clipped` (device uint32 or
  * NULL) has the number of elements the clamp changed ADDED to it.  A NaN in
@@ -262,7 +272,7 @@ sq_status sq_rmsnorm_quant_act(const void* h, sq_dtype dt, int64_t tokens, int64
  * power of two).  Z = (X S^-1) H is formed by the fast Walsh-Hadamard
  * transform, stages h = 1, 2, 4, ... in that order, each butterfly
  * (a, b) -> (a + b, a - b) one binary32 addition and subtraction.  Codes
- * clamp(rne(Z * (1/dz)), -qmax, qmax) with dz = RN(max|Z| / qmax) per row
+ * clamp(rne(Z / dz), -qmax, qmax) with dz = RN(max|Z| / qmax) per row
  * (1 if the maximum is 0); qmax = 7 gives 4-bit codes, 127 the 8-bit ones.
  * The 1/d of R R^T = H H^T / d is carried by the activation scale as the
  * exact factor 2^-log2(d): x_scale = dz * 2^-log2(d), w_scale = dz, so
@@ -302,12 +312,15 @@ sq_status sq_rotate_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin
  *   y      device bf16 [m x n] row-major
  *   acc_out  device int32 [m x n] or NULL: the exact accumulators
  *   workspace  device, >= sq_workspace_bytes(SQ_OP_GEMM, m, n, k, fmt)
- * k must be a multiple of 16.  SQ_CODES_BF16 runs on the tcgen05 tensor
+ * k must be a multiple of 16 and at most SQ_GEMM_MAX_K (beyond it a sum of
+ * k products of 127 * 127 could leave int32: SQ_ERR_UNSUPPORTED).
+ * SQ_CODES_BF16 runs on the tcgen05 tensor
  * cores (fp32 accumulation in TMEM, converted to int32 every <= 1024
  * products so every partial sum stays an exact integer); SQ_CODES_I8 runs
  * on the legacy integer mma.sync path, which suits small m (decode).
  * A pipeline wait that runs out sets SQ_FLAG_TIMEOUT.
  */
+#define SQ_GEMM_MAX_K 133136 /* largest multiple of 16 with k * 127^2 < 2^31 */
 sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq,
                        const float* w_scale, sq_codes fmt, int64_t m, int64_t n, int64_t k,
                        void* y, int32_t* acc_out, int32_t* dev_flags, void* workspace,
@@ -335,7 +348,8 @@ sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq,
  *   summed in float64; relative error ~1e-6 of |X W|).  x [tokens x cin]
  *   (ldx), w [cin x cout] (ldw), both of type dt; y bf16 [tokens x cout]
  *   contiguous; rows device int32 [nrows], 1 <= nrows <= 64; err device
- *   double [nrows] (overwritten).
+ *   double [nrows] (overwritten).  A sampled index outside [0, tokens) is
+ *   never dereferenced: its err entry is NaN.
  * sq_channel_stats: out[0] = mean, out[1] = population standard deviation
  *   of v_j = RN(amax[j] * scale[j]) (scale NULL: v_j = amax[j]); with
  *   amax = max|X_j| and scale = s_inv, the channel magnitudes after
@@ -415,6 +429,20 @@ size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fm
  */
 int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int64_t ld, int axis,
                     int accumulate);
+
+/*
+ * Read (and optionally clear) a device flag word and turn it into a status.
+ * Source: none on the pages; it is the boundary's status convention for the
+ * data-dependent conditions above.  Enqueues a 4-byte device-to-host copy of
+ * *dev_flags on `stream` (after the work already there), then, with clear =
+ * 1, zeroes the word, and waits for the stream: a synchronizing call, not
+ * for use inside stream capture.  Returns SQ_ERR_TIMEOUT if
+ * SQ_FLAG_TIMEOUT is set, else SQ_ERR_NONFINITE if SQ_FLAG_NONFINITE is
+ * set, else SQ_OK; flags_out (host, or NULL) receives the raw word.
+ *   dev_flags  device int32, 4-byte aligned;  clear  0 or 1
+ */
+sq_status sq_read_device_flags(int32_t* dev_flags, int clear, int32_t* flags_out,
+                               cudaStream_t stream);
 
 /* Static text for a status code. */
 const char* sq_status_string(sq_status status);

@@ -78,6 +78,61 @@ def make_small(p):
     return synth.make_case(name, **p)
 
 
+def division_rows(cases, cin, seed):
+    """Rows [amax, v, small filler...]: each row's maximum is amax (so its
+    scale is RN(amax / qmax)) and v a crafted element whose division and
+    reciprocal codes differ."""
+    rng = np.random.default_rng(seed)
+    x = (rng.uniform(-0.25, 0.25, size=(len(cases), cin)) * np.array([c[0] for c in cases])[:, None]).astype(F32)
+    for t, (amax, v, _, _) in enumerate(cases):
+        x[t, 0] = amax
+        x[t, 1 + t % (cin - 1)] = v
+    return x
+
+
+@pytest.mark.parametrize("codes", ["i8", "bf16"])
+def test_codes_divide_by_the_scale(sq, codes):
+    """Crafted elements whose code under rne(RN(v / d)) differs from
+    rne(RN(v * RN(1/d))): every quantizer (per token, per output channel in
+    the single-pass and the two-pass fold, static scale, low-bit rows) gives
+    the division's code."""
+    from tests.test_oracle_pins import division_split_cases
+    cases = division_split_cases(127, 96, seed=31)
+    x = division_rows(cases, 48, seed=1)
+    ones = torch.ones(48, device="cuda")
+    xq_ref, xs_ref, _ = O.quant_act(x, np.ones(48, F32))
+    for t, (_, v, want, _) in enumerate(cases):
+        assert xq_ref[t, 1 + t % 47] == want
+    xq, xs = sq.quant_act(dev(x, "f32"), ones, codes)
+    assert np.array_equal(codes_np(xq), xq_ref) and np.array_equal(f32bits(xs), npbits(xs_ref))
+    # the fold quantizes the same values per output channel (W = X^T)
+    w = np.ascontiguousarray(x.T)
+    wq_ref, ws_ref, _ = O.fold_quantize_weight(w, np.ones(48, F32))
+    assert np.array_equal(wq_ref, xq_ref)
+    wq, ws = sq.fold_quantize_weight(dev(w, "f32"), ones, codes)
+    assert np.array_equal(codes_np(wq), wq_ref) and np.array_equal(f32bits(ws), npbits(ws_ref))
+    # two-pass fold: a row stride that is not a multiple of 16 bytes
+    wpad = torch.zeros(48, 97, device="cuda")
+    wpad[:, :96] = dev(w, "f32")
+    wq2, ws2 = sq.fold_quantize_weight(wpad[:, :96], ones, codes)
+    assert np.array_equal(codes_np(wq2), wq_ref) and np.array_equal(f32bits(ws2), npbits(ws_ref))
+    # static scale: one maximum for every row
+    scases = division_split_cases(127, 64, seed=32, amax_fixed=37.25)
+    xs_rows = division_rows(scases, 48, seed=2)
+    d = torch.tensor([np.float32(37.25) / np.float32(127)], device="cuda")
+    qs_ref, _, clipped_ref = O.quant_act_static(xs_rows, np.ones(48, F32), d.item())
+    clipped = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qs, _ = sq.quant_act_static(dev(xs_rows, "f32"), ones, d, codes, clipped)
+    assert np.array_equal(codes_np(qs), qs_ref) and int(clipped.item()) == clipped_ref == 0
+    # low-bit rows (no smoothing, no rotation) with 7 and 127 levels
+    for qmax, seed in ((7, 33), (127, 34)):
+        rc = division_split_cases(qmax, 64, seed=seed)
+        xr = division_rows(rc, 64, seed=seed)
+        q_ref, s_ref, _ = O.rotate_quant_act(xr, None, False, qmax)
+        q, sc = sq.rotate_quant_act(dev(xr, "f32"), None, False, qmax, codes)
+        assert np.array_equal(codes_np(q), q_ref) and np.array_equal(f32bits(sc), npbits(s_ref))
+
+
 # ------------------------------------------------------------------ per-step parity
 @pytest.mark.parametrize("p", SMALL, ids=[p["name"] for p in SMALL])
 def test_calibrate_bit_exact(sq, p):

@@ -42,6 +42,7 @@ def test_status_strings(lib):
     assert h.sq_status_string(0) == b"ok"
     assert h.sq_status_string(1) == b"invalid argument"
     assert h.sq_status_string(99) == b"unknown status"
+    assert h.sq_status_string(6) == b"a bounded device wait ran out"
 
 
 def test_workspace_sizes(lib):
@@ -77,6 +78,22 @@ def test_argument_validation_needs_no_device(lib):
     assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 4, 4, 24, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
     assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, 0, 0, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
     assert h.sq_w8a8_gemm(odd, aligned, aligned, aligned, 0, 4, 4, 32, aligned, None, None, None, 0, None) == sq.SQ_ERR_INVALID_ARG
+    # GEMM: k beyond the int32 accumulator bound (k * 127^2 >= 2^31)
+    assert sq.SQ_GEMM_MAX_K * 127 * 127 < 2 ** 31 <= (sq.SQ_GEMM_MAX_K + 16) * 127 * 127
+    assert sq.SQ_GEMM_MAX_K % 16 == 0
+    for fmt in (0, 1):
+        assert h.sq_w8a8_gemm(aligned, aligned, aligned, aligned, fmt, 4, 4, sq.SQ_GEMM_MAX_K + 16, aligned,
+                              None, None, None, 0, None) == sq.SQ_ERR_UNSUPPORTED
+    # flag reader: null or misaligned word, bad clear argument
+    out = ctypes.c_int32(0)
+    assert h.sq_read_device_flags(None, 0, ctypes.byref(out), None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_read_device_flags(P(4098), 0, ctypes.byref(out), None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_read_device_flags(aligned, 2, ctypes.byref(out), None) == sq.SQ_ERR_INVALID_ARG
+    # layer error: too many sampled rows, zero tokens
+    assert h.sq_layer_error(aligned, aligned, sq.SQ_BF16, 4, 32, 8, 32, 8, aligned, aligned, 65, aligned,
+                            None) == sq.SQ_ERR_INVALID_ARG
+    assert h.sq_layer_error(aligned, aligned, sq.SQ_BF16, 0, 32, 8, 32, 8, aligned, aligned, 4, aligned,
+                            None) == sq.SQ_ERR_INVALID_ARG
     # whole path from host memory: null host buffer, cin % 16, missing device buffer, workspace
     full = {n: type("T", (), {"data_ptr": lambda self: 4096})() for n in
             ("x", "w", "amax_x", "amax_w", "s", "s_inv", "wq", "w_scale", "xq", "x_scale", "y")}
@@ -123,3 +140,20 @@ def test_host_binding_checks_shapes_and_dtypes(lib):
         sq.linear_host(x, torch.zeros(16, 8, dtype=torch.bfloat16), 0.5, "i8", y, b)
     with pytest.raises(ValueError):  # Y is not tokens x cout
         sq.linear_host(x, torch.zeros(32, 8, dtype=torch.bfloat16), 0.5, "i8", torch.zeros(4, 9, dtype=torch.bfloat16), b)
+
+
+def test_layer_error_binding_rejects_rows_outside_the_tokens(lib, monkeypatch):
+    """A sampled token index outside [0, tokens), or an output of the wrong
+    shape, is refused on the host before anything reaches the device."""
+    import torch
+    from w8a8_post_quantization_02_b300 import sq
+    monkeypatch.setattr(sq, "_check_cuda_2d", lambda t, name: None)
+    x = torch.zeros(4, 32, dtype=torch.bfloat16)
+    w = torch.zeros(32, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sq.layer_error(x, w, y, torch.tensor([0, 4]))
+    with pytest.raises(ValueError):
+        sq.layer_error(x, w, y, torch.tensor([-1]))
+    with pytest.raises(ValueError):
+        sq.layer_error(x, w, torch.zeros(3, 8, dtype=torch.bfloat16), torch.tensor([0]))

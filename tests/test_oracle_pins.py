@@ -240,16 +240,19 @@ def test_rne_ties_and_clamp():
     assert q.tolist() == [[2, 4, -2, 0, 2, -127, 127, 126, 0]]
 
 
-def division_split_cases(qmax, count, seed):
-    """Pairs (amax, v) with |v| < amax where the code of v under the scale
-    d = RN(amax / qmax), rne(RN(v / d)), differs from the code a reciprocal
-    would give, rne(RN(v * RN(1 / d))).  Found and decided in exact rational
-    arithmetic (no binary32 division is used), next to half-integer
-    multiples of d, where the two roundings can part."""
+def division_split_cases(qmax, count, seed, amax_fixed=None):
+    """Tuples (amax, v, code, reciprocal code) with |v| < amax where the
+    code of v under the scale d = RN(amax / qmax), rne(RN(v / d)), differs
+    from the code a reciprocal would give, rne(RN(v * RN(1 / d))).  Found
+    and decided in exact rational arithmetic (no binary32 division is used),
+    next to half-integer multiples of d, where the two roundings can part.
+    ``amax_fixed`` keeps one maximum (one scale) for every case."""
     rng = np.random.default_rng(seed)
     out = []
-    while len(out) < count:
-        amax = F32(rng.uniform(0.5, 100.0))
+    for _ in range(100000):
+        if len(out) >= count:
+            break
+        amax = F32(amax_fixed) if amax_fixed is not None else F32(rng.uniform(0.5, 100.0))
         d = rn32(Fr(float(amax)) / qmax)
         inv = rn32(1 / d)
         k = int(rng.integers(0, qmax)) + Fr(1, 2)
@@ -266,6 +269,7 @@ def division_split_cases(qmax, count, seed):
                 sign = -1 if len(out) % 2 else 1
                 out.append((amax, F32(sign * v), sign * by_div, sign * by_rcp))
                 break
+    assert len(out) == count, "too few crafted cases found"
     return out
 
 

@@ -13,7 +13,8 @@
 // Every thread owns the same column vectors of every row and keeps their
 // s^-1 in registers.  Pass 1 forms X' = X * s^-1 (kept in registers) and
 // the row's max|X'|; one block barrier combines the warps' maxima (and
-// frees the stage for the next copy); pass 2 writes the codes.  HBM
+// frees the stage for the next copy); pass 2 writes the codes
+// rne(RN(X' / d)), the binary32 quotient formed by quot_rn.  HBM
 // traffic per element: one read of X and one write of the code, plus 4
 // bytes per token for the scale.  The same kernel serves the static
 // variant (one calibrated scale for every token, SmoothQuant glossary:
@@ -229,9 +230,11 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
   }
 
   float d_fix = 1.0f, inv_fix = 1.0f;
+  bool fast_fix = false;
   if constexpr (STATIC) {
     d_fix = *d_static;
     inv_fix = __fdiv_rn(1.0f, d_fix);
+    fast_fix = fast_scale_ok(d_fix);
   }
   uint32_t nclip = 0u;
   bool nonfinite = false;
@@ -394,13 +397,13 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
         x_scale[r] = d;
         if (!finite_bits(amax)) raise_flag(flags, SQ_FLAG_NONFINITE);
       }
-      // With a finite max >= 2^-119, d = RN(amax/127) and 1/d are normal, so
-      // |X' * (1/d)| <= 127 * (1 + 3 * 2^-24) < 127.5 and the clamp to
-      // [-127, 127] can never change a code: it is skipped.
-      no_clamp = amax >= 0x04000000u && amax < 0x7F800000u;
+      // With a finite max >= 2^-93 the quotient X'/d comes from quot_rn and
+      // no code can leave [-127, 127], so the clamp is skipped; any other
+      // row (tiny, zero or non-finite maximum) divides element by element.
+      no_clamp = fast_quotient_ok(amax);
     }
 
-    // pass 2: codes = rne(X' * (1/d)), via the magic-number add
+    // pass 2: codes = rne(RN(X' / d)), via the magic-number add
     uint8_t* qrow = xq + r * (int64_t)nvec * E * CB;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -408,17 +411,17 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
       if (v >= nvec) continue;
       float q[E];
       if (no_clamp) {
-        // scalar multiply and add, each with its own rounding: ptxas does
-        // not contract mul.rn/add.rn into a fused multiply-add, which would
-        // round ties of X'/d differently from rne(RN(X' * (1/d)))
 #pragma unroll
-        for (int e = 0; e < E; ++e) q[e] = __fadd_rn(__fmul_rn(p[i][e], inv), kMagic);
+        for (int e = 0; e < E; ++e) q[e] = magic_of(quot_rn(p[i][e], d, inv));
       } else if constexpr (STATIC) {
-        // scalar multiply, clamp, then the rounding add.  A NaN gives code 0
-        // and +-inf saturates; neither counts as clipped, both are flagged.
+        // the quotient (quot_rn inside its range, else an IEEE division),
+        // clamp, then the rounding add.  A NaN gives code 0 and +-inf
+        // saturates; neither counts as clipped, both are flagged.
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const float t = __fmul_rn(p[i][e], inv);
+          const float q0 = __fmul_rn(p[i][e], inv);
+          const float t = (fast_fix && fabsf(q0) < 256.0f) ? quot_refine(p[i][e], d, inv, q0)
+                                                           : __fdiv_rn(p[i][e], d);
           const float a = fabsf(t);
           const bool finite = a <= 3.4028234663852886e38f;
           nonfinite |= !finite;
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) q[e] = code_magic(p[i][e], inv);
+        for (int e = 0; e < E; ++e) q[e] = code_div_magic(p[i][e], d, 127.0f);
       }
       if constexpr (CODES == SQ_CODES_BF16) {
         uint32_t w[E / 2];

@@ -28,7 +28,7 @@ sq_status act_quant_error(const void*, sq_dtype, int64_t, int64_t, int64_t, cons
 sq_status weight_quant_error(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*,
                              const void*, sq_codes, const float*, double*, cudaStream_t);
 int layer_error_max_rows();
-sq_status layer_error(const void*, const void*, sq_dtype, int64_t, int64_t, int64_t, int64_t,
+sq_status layer_error(const void*, const void*, sq_dtype, int64_t, int64_t, int64_t, int64_t, int64_t,
                       const void*, const int32_t*, int, double*, cudaStream_t);
 sq_status channel_stats(const float*, const float*, int64_t, double*, cudaStream_t);
 int calibrate_kernel_count(sq_dtype, int64_t, int64_t, int64_t, int, int);
@@ -56,8 +56,24 @@ const char* sq_status_string(sq_status s) {
     case SQ_ERR_CUDA: return "CUDA error";
     case SQ_ERR_UNSUPPORTED: return "unsupported request";
     case SQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case SQ_ERR_TIMEOUT: return "a bounded device wait ran out";
   }
   return "unknown status";
+}
+
+sq_status sq_read_device_flags(int32_t* dev_flags, int clear, int32_t* flags_out,
+                               cudaStream_t stream) {
+  if (!dev_flags || (clear != 0 && clear != 1) || (reinterpret_cast<uintptr_t>(dev_flags) & 3))
+    return SQ_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_flags, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return SQ_ERR_CUDA;
+  if (clear && cudaMemsetAsync(dev_flags, 0, sizeof(v), stream) != cudaSuccess) return SQ_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SQ_ERR_CUDA;
+  if (flags_out) *flags_out = v;
+  if (v & SQ_FLAG_TIMEOUT) return SQ_ERR_TIMEOUT;
+  if (v & SQ_FLAG_NONFINITE) return SQ_ERR_NONFINITE;
+  return SQ_OK;
 }
 
 sq_status sq_check_device(int device) {
@@ -245,7 +261,6 @@ sq_status sq_weight_quant_error(const void* w, sq_dtype dt, int64_t cin, int64_t
 sq_status sq_layer_error(const void* x, const void* w, sq_dtype dt, int64_t tokens, int64_t cin,
                          int64_t cout, int64_t ldx, int64_t ldw, const void* y,
                          const int32_t* rows, int nrows, double* err, cudaStream_t stream) {
-  (void)tokens;
   if (!x || !w || !y || !rows || !err || !valid_dtype(dt) || tokens < 1 || cin < 1 || cout < 1 ||
       ldx < cin || ldw < cout || nrows < 1 || nrows > layer_error_max_rows())
     return SQ_ERR_INVALID_ARG;
@@ -253,7 +268,7 @@ sq_status sq_layer_error(const void* x, const void* w, sq_dtype dt, int64_t toke
       (reinterpret_cast<uintptr_t>(w) % elem_bytes(dt)) != 0 || (reinterpret_cast<uintptr_t>(y) & 1) ||
       (reinterpret_cast<uintptr_t>(rows) & 3) || (reinterpret_cast<uintptr_t>(err) & 7))
     return SQ_ERR_INVALID_ARG;
-  return layer_error(x, w, dt, cin, cout, ldx, ldw, y, rows, nrows, err, stream);
+  return layer_error(x, w, dt, tokens, cin, cout, ldx, ldw, y, rows, nrows, err, stream);
 }
 
 sq_status sq_channel_stats(const float* amax, const float* scale, int64_t n, double* out,
@@ -271,6 +286,7 @@ sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq, con
   if (!xq || !x_scale || !wq || !w_scale || !y || !valid_codes(fmt) || m < 1 || n < 1 || k < 16 ||
       k % 16 != 0)
     return SQ_ERR_INVALID_ARG;
+  if (k > SQ_GEMM_MAX_K) return SQ_ERR_UNSUPPORTED;  // int32 accumulators could wrap
   if (!aligned16(xq) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(y) & 3) ||
       (reinterpret_cast<uintptr_t>(acc_out) & 3))
     return SQ_ERR_INVALID_ARG;

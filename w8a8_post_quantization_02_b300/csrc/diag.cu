@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(256) k_layer_error(const uint8_t* __restrict__
                                                      int64_t ldw_bytes,
                                                      const __nv_bfloat16* __restrict__ y,
                                                      const int32_t* __restrict__ rows, int nrows,
-                                                     double* __restrict__ err) {
+                                                     int64_t tokens, double* __restrict__ err) {
   constexpr int EB = BF16 ? 2 : 4;
   __shared__ float xs[kMaxRows][kJ + 1];
   __shared__ float wsm[kJ][kT + 1];
@@ -171,7 +171,9 @@ __global__ void __launch_bounds__(256) k_layer_error(const uint8_t* __restrict__
     for (int i = tid; i < kMaxRows * kJ; i += 256) {
       const int r = i / kJ, jl = i % kJ;
       const int64_t j = j0 + jl;
-      xs[r][jl] = (r < nrows && j < cin) ? load(x + (int64_t)rows[r] * ldx_bytes + j * EB) : 0.0f;
+      // a sampled index outside [0, tokens) is never dereferenced
+      const bool ok = r < nrows && j < cin && rows[r] >= 0 && rows[r] < tokens;
+      xs[r][jl] = ok ? load(x + (int64_t)rows[r] * ldx_bytes + j * EB) : 0.0f;
     }
     for (int i = tid; i < kJ * kT; i += 256) {
       const int jl = i / kT, c = i % kT;
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(256) k_layer_error(const uint8_t* __restrict__
   for (int i = 0; i < 16; ++i) {
     const int r = rg * 16 + i;
     double sq = 0.0;
-    if (r < nrows && n < cout) {
+    if (r < nrows && n < cout && rows[r] >= 0 && rows[r] < tokens) {
       const double diff = acc[i] - (double)__bfloat162float(y[(int64_t)rows[r] * cout + n]);
       sq = diff * diff;
     }
@@ -205,7 +207,12 @@ __global__ void __launch_bounds__(256) k_layer_error(const uint8_t* __restrict__
     if (lane == 0) red[r][(tid >> 5) & 1] = sq;
   }
   __syncthreads();
-  if (tid < nrows) atomicAdd(&err[tid], red[tid][0] + red[tid][1]);
+  if (tid < nrows) {
+    if (rows[tid] >= 0 && rows[tid] < tokens)
+      atomicAdd(&err[tid], red[tid][0] + red[tid][1]);
+    else
+      err[tid] = __longlong_as_double(0x7FF8000000000000ll);  // NaN: no such token
+  }
 }
 
 // out = (mean, population std) of v_j = RN(amax[j] * scale[j]) (scale may be null).
@@ -282,9 +289,9 @@ sq_status weight_quant_error(const void* w, sq_dtype dt, int64_t cin, int64_t co
 
 int layer_error_max_rows() { return kMaxRows; }
 
-sq_status layer_error(const void* x, const void* w, sq_dtype dt, int64_t cin, int64_t cout,
-                      int64_t ldx, int64_t ldw, const void* y, const int32_t* rows, int nrows,
-                      double* err, cudaStream_t st) {
+sq_status layer_error(const void* x, const void* w, sq_dtype dt, int64_t tokens, int64_t cin,
+                      int64_t cout, int64_t ldx, int64_t ldw, const void* y, const int32_t* rows,
+                      int nrows, double* err, cudaStream_t st) {
   if (cudaMemsetAsync(err, 0, sizeof(double) * nrows, st) != cudaSuccess) return SQ_ERR_CUDA;
   const unsigned grid = (unsigned)((cout + kT - 1) / kT);
   const int eb = elem_bytes(dt);
@@ -292,9 +299,9 @@ sq_status layer_error(const void* x, const void* w, sq_dtype dt, int64_t cin, in
   const uint8_t* wb = static_cast<const uint8_t*>(w);
   const __nv_bfloat16* yb = static_cast<const __nv_bfloat16*>(y);
   if (dt == SQ_BF16)
-    k_layer_error<true><<<grid, 256, 0, st>>>(xb, wb, cin, cout, ldx * eb, ldw * eb, yb, rows, nrows, err);
+    k_layer_error<true><<<grid, 256, 0, st>>>(xb, wb, cin, cout, ldx * eb, ldw * eb, yb, rows, nrows, tokens, err);
   else
-    k_layer_error<false><<<grid, 256, 0, st>>>(xb, wb, cin, cout, ldx * eb, ldw * eb, yb, rows, nrows, err);
+    k_layer_error<false><<<grid, 256, 0, st>>>(xb, wb, cin, cout, ldx * eb, ldw * eb, yb, rows, nrows, tokens, err);
   return launch_status();
 }
 

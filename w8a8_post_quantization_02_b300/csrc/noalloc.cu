@@ -27,14 +27,24 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_fold_scratch on the current device, looked up once per
-// device.  In host code the array's name only stands in for the device
-// symbol, so the address must come from cudaGetSymbolAddress.
-sq_status scratch_address(void** out) {
+// Device address of g_fold_scratch on the current device.  In host code the
+// array's name only stands in for the device symbol, so the address must
+// come from cudaGetSymbolAddress.  Outside stream capture it is looked up
+// on every call (cheap once the module is loaded), so a device reset, which
+// reloads the module and may move the array, never leaves a stale address;
+// a call made while `stream` is capturing reuses the last address seen on
+// this device, since capture forbids the module loading a first lookup may
+// need.
+sq_status scratch_address(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SQ_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return SQ_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone || !g_scratch_addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_fold_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();  // reset the runtime's last-error state for later calls
@@ -61,7 +71,7 @@ extern "C" sq_status sq_fold_quantize_weight_noalloc(const void* w, sq_dtype dt,
     return SQ_ERR_INVALID_ARG;
   if (cout > SQ_NOALLOC_MAX_COUT) return SQ_ERR_WORKSPACE;  // beyond the fixed scratch
   void* scratch = nullptr;
-  const sq_status st = sq::scratch_address(&scratch);
+  const sq_status st = sq::scratch_address(stream, &scratch);
   if (st != SQ_OK) return st;
   // the fold zeroes the cout maxima it uses before accumulating into them
   return sq::fold_quantize_weight(w, dt, cin, cout, ldw, s, wq, fmt, w_scale, dev_flags, scratch,

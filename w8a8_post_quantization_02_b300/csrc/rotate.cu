@@ -14,7 +14,7 @@
 // (a + b, a - b) in binary32): stages inside a vector in registers, across
 // lanes by warp shuffles, across warps through shared memory, across a
 // thread's vectors in registers.  The row's max|Z| gives the scale
-// d = RN(max|Z| / qmax) and codes clamp(rne(Z * (1/d)), -qmax, qmax).
+// d = RN(max|Z| / qmax) and codes clamp(rne(RN(Z / d)), -qmax, qmax).
 // The 1/d_len of R R^T = H H^T / d_len rides on the activation scale as the
 // exact power of two 2^-L.  The same kernel quantizes the rows of the
 // transposed, folded weight (k_fold_transpose), one row per output channel.
@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(1024) k_rotate_rows(const uint8_t* __restrict_
     const float am = __uint_as_float(amax);
     const float d = (amax == 0u) ? 1.0f : __fdiv_rn(am, qmax);
     const float inv = __fdiv_rn(1.0f, d);
+    const bool fast = fast_quotient_ok(amax);  // then no code leaves [-qmax, qmax]
     if (tid == 0) {
       row_scale[r] = log2_len ? ldexpf(d, -log2_len) : d;
       if (!finite_bits(amax)) raise_flag(flags, SQ_FLAG_NONFINITE);
@@ -165,10 +166,12 @@ __global__ void __launch_bounds__(1024) k_rotate_rows(const uint8_t* __restrict_
       const int v = tid + i * nt;
       if (v >= nvec) continue;
       float c[E];
+      if (fast) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float t = __fmul_rn(f[i][e], inv);
-        c[e] = __fadd_rn((t == t) ? fminf(fmaxf(t, -qmax), qmax) : 0.0f, kMagic);
+        for (int e = 0; e < E; ++e) c[e] = magic_of(quot_rn(f[i][e], d, inv));
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) c[e] = code_div_magic(f[i][e], d, qmax);
       }
       if constexpr (CODES == SQ_CODES_BF16) {
         uint32_t w[E / 2];

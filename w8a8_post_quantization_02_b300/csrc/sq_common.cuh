@@ -100,21 +100,63 @@ SQ_DEVINL void raise_flag(int32_t* flags, int32_t bit) {
 SQ_DEVINL bool finite_bits(uint32_t absb) { return absb < 0x7F800000u; }
 
 // Symmetric INT8 scale for a maximum magnitude: d = amax / 127 (IEEE fp32
-// division), 1 when amax == 0, and its reciprocal 1/d (IEEE division).
+// division), 1 when amax == 0, and its reciprocal RN(1/d) (IEEE division),
+// which the quotient below refines.
 SQ_DEVINL void scale_and_inverse(float amax, float& d, float& inv) {
   d = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
   inv = __fdiv_rn(1.0f, d);
 }
 
-// rne(clamp(v * inv, -127, 127)) returned as the float v' = code + 1.5*2^23,
-// whose low byte is the two's-complement code and whose value minus
-// 1.5*2^23 is the code exactly.  The add rounds to nearest-even on the
-// integer grid because 1.5*2^23 + [-127.5, 127.5] lies in [2^23, 2^24).
+// The quantizer's code is rne(RN(v / d)): the IEEE binary32 quotient,
+// rounded to the nearest integer.  quot_rn forms that quotient with one
+// multiply and four fused multiply-adds instead of a division:
+//   q0 = RN(v * y)                     y = RN(1/d), so |q0 - v/d| < 1.5 ulp
+//   q1 = RN(q0 + RN(v - d q0) * y)     |q1 - v/d| < 1 ulp (faithful)
+//   q2 = RN(q1 + (v - d q1) * y)       the remainder v - d q1 is exact
+// and q2 = RN(v / d) by Markstein's theorem (P. Markstein, IBM J. Res. Dev.
+// 34(1), 1990; also Cornea, Harrison and Tang, "Scientific Computing on
+// Itanium-based Systems", 2002): with y correctly rounded and q1 faithful,
+// one residual correction gives the correctly rounded quotient.  Its
+// premises hold when d lies in [2^-100, 2^120] and |v / d| <= 256: then
+// no product, remainder or correction leaves the normal range (a remainder
+// is a multiple of 2^(e_d + e_q - 46) >= 2^-148 whenever |v / d| >= 2^-2,
+// and below that every candidate rounds to code 0).  Every caller checks
+// those bounds and otherwise takes __fdiv_rn.
+SQ_DEVINL float quot_refine(float v, float d, float y, float q0) {
+  const float r0 = __fmaf_rn(-d, q0, v);
+  const float q1 = __fmaf_rn(r0, y, q0);
+  const float r1 = __fmaf_rn(-d, q1, v);
+  return __fmaf_rn(r1, y, q1);
+}
+SQ_DEVINL float quot_rn(float v, float d, float y) { return quot_refine(v, d, y, __fmul_rn(v, y)); }
+
+// A row or channel maximum at or above 2^-93 (and finite) gives
+// d = RN(amax / qmax) >= 2^-100 for any qmax <= 127, inside quot_rn's range;
+// and since every |v| <= amax, |v / d| <= qmax * (1 + 2^-23), whose
+// rounding to an integer never exceeds qmax: no clamp is needed.
+constexpr uint32_t kFastAmaxBits = 0x11000000u;  // 2^-93
+SQ_DEVINL bool fast_quotient_ok(uint32_t amax_bits) {
+  return amax_bits >= kFastAmaxBits && amax_bits < 0x7F800000u;
+}
+// d within quot_rn's range, for a scale not derived from the values it
+// divides (the static activation scale): [2^-100, 2^120].
+SQ_DEVINL bool fast_scale_ok(float d) {
+  const uint32_t b = __float_as_uint(d);
+  return b >= 0x0D800000u && b <= 0x7B800000u;
+}
+
+// rne(q) returned as the float q' = code + 1.5*2^23, whose low byte is the
+// two's-complement code and whose value minus 1.5*2^23 is the code
+// exactly.  The add rounds to nearest-even on the integer grid because
+// 1.5*2^23 + [-127.5, 127.5] lies in [2^23, 2^24).
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-SQ_DEVINL float code_magic(float v, float inv) {
-  float q = __fmul_rn(v, inv);
-  q = fminf(fmaxf(q, -127.0f), 127.0f);
-  return __fadd_rn(q, kMagic);
+SQ_DEVINL float magic_of(float q) { return __fadd_rn(q, kMagic); }
+
+// clamp(rne(RN(v / d)), -qmax, qmax) as a magic float, for any v and d:
+// one IEEE division; a NaN quotient gives code 0, +-inf saturates.
+SQ_DEVINL float code_div_magic(float v, float d, float qmax) {
+  const float t = __fdiv_rn(v, d);
+  return __fadd_rn((t == t) ? fminf(fmaxf(t, -qmax), qmax) : 0.0f, kMagic);
 }
 
 SQ_DEVINL uint32_t magic_to_bf16bits(float m) {

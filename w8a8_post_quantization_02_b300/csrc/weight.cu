@@ -138,21 +138,26 @@ __global__ void __launch_bounds__(kThreads) k_fold_quant(const uint8_t* __restri
                                                          int32_t* flags) {
   constexpr int CB = CODES == SQ_CODES_BF16 ? 2 : 1;
   constexpr int ROWB = TJ * CB + 16;  // padded bytes per output-channel row of the tile
-  __shared__ float inv_s[TN];
+  __shared__ float d_s[TN], inv_s[TN];
+  __shared__ bool fast_s[TN];
   __shared__ __align__(16) uint8_t tile[TN * ROWB];
   const int64_t j0 = (int64_t)blockIdx.y * TJ, n0 = (int64_t)blockIdx.x * TN;
   if (threadIdx.x < TN) {
     const int64_t n = n0 + threadIdx.x;
     float d = 1.0f, inv = 1.0f;
+    bool fast = true;
     if (n < cout) {
       const uint32_t ab = amax_bits[n];
       scale_and_inverse(__uint_as_float(ab), d, inv);
+      fast = fast_quotient_ok(ab);
       if (blockIdx.y == 0) {
         w_scale[n] = d;
         if (!finite_bits(ab)) raise_flag(flags, SQ_FLAG_NONFINITE);
       }
     }
+    d_s[threadIdx.x] = d;
     inv_s[threadIdx.x] = inv;
+    fast_s[threadIdx.x] = fast;
   }
   __syncthreads();
   // each thread: 2 (row j, 8-column group) items of the 64 x 64 tile
@@ -172,7 +177,9 @@ __global__ void __launch_bounds__(kThreads) k_fold_quant(const uint8_t* __restri
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float m = code_magic(__fmul_rn(sj, f[e]), inv_s[g * 8 + e]);
+      const int ch = g * 8 + e;
+      const float v = __fmul_rn(sj, f[e]);
+      const float m = fast_s[ch] ? magic_of(quot_rn(v, d_s[ch], inv_s[ch])) : code_div_magic(v, d_s[ch], 127.0f);
       uint8_t* dst = tile + (g * 8 + e) * ROWB + jl * CB;
       if constexpr (CODES == SQ_CODES_BF16)
         *reinterpret_cast<uint16_t*>(dst) = (uint16_t)magic_to_bf16bits(m);
@@ -233,14 +240,15 @@ SQ_DEVINL void unpack_chunk(uint4 v, float* f) {
 template <int EPC>
 struct Layout {
   static constexpr int SW = 4 * EPC;  // output channels per strip
-  size_t strip, s, red, part, inv, flag, bars, total;
+  size_t strip, s, red, part, inv, dsc, flag, bars, total;
   explicit __host__ __device__ Layout(int rows_per_cta) {
     strip = 0;                                     // 1024-aligned base
     s = strip + (size_t)rows_per_cta * kRowBytes;  // fp32 [R]
     red = s + (size_t)rows_per_cta * 4;            // u32 [8 warps][4 chunks][EPC]
     part = red + 8 * 4 * EPC * 4;                  // u32 [SW], read by the whole cluster
-    inv = part + SW * 4;                           // fp32 [SW]
-    flag = inv + SW * 4;                           // int: some channel needs the clamp
+    inv = part + SW * 4;                           // fp32 [SW]: RN(1/d)
+    dsc = inv + SW * 4;                            // fp32 [SW]: d
+    flag = dsc + SW * 4;                           // int: some channel needs the division
     bars = (flag + 4 + 7) & ~size_t(7);            // mbarriers [kMaxBoxes]
     total = bars + kMaxBoxes * 8;
   }
@@ -267,6 +275,7 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
   uint32_t* red = reinterpret_cast<uint32_t*>(base + L.red);
   uint32_t* part = reinterpret_cast<uint32_t*>(base + L.part);
   float* inv_sm = reinterpret_cast<float*>(base + L.inv);
+  float* d_sm = reinterpret_cast<float*>(base + L.dsc);
   int* clamp_flag = reinterpret_cast<int*>(base + L.flag);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
 
@@ -353,11 +362,12 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
     float d, inv;
     scale_and_inverse(__uint_as_float(v), d, inv);
     inv_sm[tid] = inv;
+    d_sm[tid] = d;
     const int64_t n = n0 + tid;
     if (n < cout) {
-      // a finite maximum >= 2^-119 keeps |W' / d| below 127.5, so the clamp
-      // cannot change a code (see the activation kernel)
-      if (!(v >= 0x04000000u && v < 0x7F800000u)) *clamp_flag = 1;
+      // a finite maximum >= 2^-93: the quotient W'/d comes from quot_rn and
+      // no code leaves [-127, 127]; otherwise the CTA divides and clamps
+      if (!fast_quotient_ok(v)) *clamp_flag = 1;
       if (rank == 0) {
         w_scale[n] = d;
         if (!finite_bits(v)) raise_flag(flags, SQ_FLAG_NONFINITE);
@@ -372,9 +382,12 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
   {
     const int c = tid & 3;
     const bool clamp = *clamp_flag != 0;
-    float inv[EPC];
+    float inv[EPC], dch[EPC];
 #pragma unroll
-    for (int e = 0; e < EPC; ++e) inv[e] = inv_sm[c * EPC + e];
+    for (int e = 0; e < EPC; ++e) {
+      inv[e] = inv_sm[c * EPC + e];
+      dch[e] = d_sm[c * EPC + e];
+    }
     for (int g = tid >> 2; g * 8 < rows; g += kThreads / 4) {
       constexpr int WPC = CODES == SQ_CODES_BF16 ? 4 : 2;  // 32-bit words per channel
       uint32_t out[EPC][WPC];
@@ -389,13 +402,11 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
 #pragma unroll
           for (int e = 0; e < EPC; e += 2) mul2_rn(q[k][e], q[k][e + 1], sj, sj);
           if (!clamp) {
-            // scalar multiply then add (never contracted into a fused
-            // multiply-add, which would round ties differently)
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) q[k][e] = __fadd_rn(__fmul_rn(q[k][e], inv[e]), kMagic);
+            for (int e = 0; e < EPC; ++e) q[k][e] = magic_of(quot_rn(q[k][e], dch[e], inv[e]));
           } else {
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) q[k][e] = code_magic(q[k][e], inv[e]);
+            for (int e = 0; e < EPC; ++e) q[k][e] = code_div_magic(q[k][e], dch[e], 127.0f);
           }
         }
 #pragma unroll

@@ -15,7 +15,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsq_b300.so")
 
-SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_NONFINITE, SQ_ERR_CUDA, SQ_ERR_UNSUPPORTED, SQ_ERR_WORKSPACE = range(6)
+(SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_NONFINITE, SQ_ERR_CUDA, SQ_ERR_UNSUPPORTED, SQ_ERR_WORKSPACE,
+ SQ_ERR_TIMEOUT) = range(7)
+SQ_GEMM_MAX_K = 133136
 SQ_FLAG_NONFINITE, SQ_FLAG_TIMEOUT = 1, 2
 SQ_F32, SQ_BF16 = 0, 1
 SQ_CODES_I8, SQ_CODES_BF16 = 0, 1
@@ -55,6 +57,7 @@ SIGNATURES = {
     "sq_channel_stats": (_I32, [_P, _P, _I64, _P, _P]),
     "sq_linear_host": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _F, _I32, _P, ctypes.POINTER(LinearBuffers),
                               _P, _P]),
+    "sq_read_device_flags": (_I32, [_P, _I32, ctypes.POINTER(ctypes.c_int32), _P]),
     "sq_status_string": (ctypes.c_char_p, [_I32]),
     "sq_check_device": (_I32, [_I32]),
 }
@@ -342,13 +345,28 @@ def layer_error(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, rows: torch.T
     _check_cuda_2d(w, "w")
     tokens, cin = x.shape
     cout = w.shape[1]
+    if tuple(y.shape) != (tokens, cout) or y.dtype != torch.bfloat16:
+        raise ValueError(f"y must be bf16 [{tokens} x {cout}], got {y.dtype} {tuple(y.shape)}")
     rows = rows.to(device=x.device, dtype=torch.int32).contiguous()
+    if rows.numel() and (int(rows.min()) < 0 or int(rows.max()) >= tokens):
+        raise ValueError(f"sampled rows must lie in [0, {tokens})")
     err = torch.empty(rows.numel(), device=x.device, dtype=torch.float64)
     st = load_library().sq_layer_error(_ptr(x), _ptr(w), _dtype_code(x), tokens, cin, cout, x.stride(0),
                                        w.stride(0), _ptr(y.contiguous()), _ptr(rows), rows.numel(),
                                        _ptr(err), _stream(stream))
     _check("sq_layer_error", st)
     return err
+
+
+def read_device_flags(flags: torch.Tensor, clear: bool = False, stream=None):
+    """Synchronize `stream`, read the device flag word (optionally zeroing
+    it) and return (status, raw word): SQ_ERR_TIMEOUT, SQ_ERR_NONFINITE or
+    SQ_OK."""
+    out = ctypes.c_int32(0)
+    st = load_library().sq_read_device_flags(_ptr(flags), int(clear), ctypes.byref(out), _stream(stream))
+    if st in (SQ_ERR_INVALID_ARG, SQ_ERR_CUDA):
+        _check("sq_read_device_flags", st)
+    return st, out.value
 
 
 def channel_stats(amax: torch.Tensor, scale: torch.Tensor | None = None, stream=None):
