@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--codes", choices=["auto", "i8", "bf16"], default="auto",
+                    help="storage of the INT8 codes: one byte each (i8), the same integers as exact "
+                         "bf16 values (bf16), or the library's choice for the token count (auto)")
     ap.add_argument("--act-scale", choices=["dynamic", "static", "norm"], default="dynamic",
                     help="per-token scales (default), one calibrated scale per tensor, or per-token "
                          "scales after an RMS normalization whose gain absorbs S^-1 (the workload's X "
@@ -169,22 +172,36 @@ def oracle_sample_case(case, tokens: int):
                       cout=case.cout, alpha=case.alpha, x=x, w=case.w, splits=case.splits)
 
 
-def time_oracle(case, budget_s: float, sample_tokens: int, max_steps: int):
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def time_oracle(case, budget_s: float, sample_tokens: int, max_steps: int, threads: int | None = None):
     """Run the oracle's whole path on a token sample of the layer (full W)
-    until ``max_steps`` runs or ``budget_s`` seconds are used."""
+    until ``max_steps`` runs or ``budget_s`` seconds are used, with the BLAS
+    library (the oracle's one multi-threaded primitive, the accumulator
+    matmul) limited to ``threads`` (default: every core this process may
+    use).  Returns (times, ops, threads used)."""
     from oracle import sq_oracle as O
+    from threadpoolctl import threadpool_limits
+    n = threads or host_cores()
     sc = oracle_sample_case(case, sample_tokens)
     x, w = sc.x_f32(), sc.w_f32()
     times = []
-    t_start = time.perf_counter()
-    while len(times) < max_steps:
-        t0 = time.perf_counter()
-        O.run_path(x, w, sc.alpha)
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_start > budget_s:
-            break
+    with threadpool_limits(limits=n, user_api="blas"):
+        t_start = time.perf_counter()
+        while len(times) < max_steps:
+            t0 = time.perf_counter()
+            O.run_path(x, w, sc.alpha)
+            times.append(time.perf_counter() - t0)
+            if time.perf_counter() - t_start > budget_s:
+                break
+        used = blas_threads()
     ops = 2 * sample_tokens * case.cin * case.cout
-    return times, ops
+    return times, ops, used
 
 
 def run_reference(args, case_name):
@@ -196,10 +213,9 @@ def run_reference(args, case_name):
     sample_tokens = min(case.tokens, 256)
     # warm-up runs (untimed), then the timed steps within a few minutes
     time_oracle(case, 0.0, sample_tokens, max(1, min(args.warmup, 1)))
-    times, ops = time_oracle(case, 150.0, sample_tokens, args.steps)
+    times, ops, cores = time_oracle(case, 150.0, sample_tokens, args.steps)
     sec = sum(times)
     value = ops * len(times) / sec / 1e12
-    cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
         "steps": len(times), "warmup": args.warmup, "ms_per_step": sec / len(times) * 1e3,
@@ -250,7 +266,8 @@ def run_ours(args, case_name):
     peaks, peaks_kind = load_peaks()
     case = synth.workload(case_name)
     x_host, w_host = to_device(case, torch)
-    layer = pipeline.Layer.for_case(case, act_scale=args.act_scale)
+    layer = pipeline.Layer.for_case(case, codes=None if args.codes == "auto" else args.codes,
+                                    act_scale=args.act_scale)
     layer.load(x_host.cuda(), w_host.cuda())
     stream = torch.cuda.current_stream()
     st = sq._stream(stream)
@@ -309,6 +326,7 @@ def run_ours(args, case_name):
 
     # each kernel alone, L2 flushed before it: its HBM roofline fraction
     nbytes = layer.algorithmic_bytes()
+    sbytes = layer.storage_bytes()
     hbm = float(peaks["hbm_gbs"])
     iso = {}
     reps = 20
@@ -316,9 +334,11 @@ def run_ours(args, case_name):
         e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         for a, b in e:
             flush_l2()
-            # hold the stream for ~50 us so the host has enqueued the
-            # kernel before the start event fires (no host gap is timed)
-            torch.cuda._sleep(100000)
+            # hold the stream for ~0.5 ms so the host has enqueued the
+            # kernel before the start event fires (no host gap is timed;
+            # with a 50 us hold the X-absmax figure ran 9 us above the
+            # profiler's time for the same launch)
+            torch.cuda._sleep(1000000)
             a.record(stream)
             fn(st)
             b.record(stream)
@@ -329,18 +349,23 @@ def run_ours(args, case_name):
         us = float(np.mean([a.elapsed_time(b) for a, b in e])) * 1e3
         gbs = nbytes[name] / (us * 1e-6) / 1e9
         iso[name] = {"us": round(us, 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
+        if sbytes[name] != nbytes[name]:  # codes stored as bf16: the bytes actually moved
+            iso[name]["storage_gbs"] = round(sbytes[name] / (us * 1e-6) / 1e9, 1)
     iso["gemm"]["tops"] = round(ops / (iso["gemm"]["us"] * 1e-6) / 1e12, 2)
     act_stage = {"dynamic": "quant_act", "static": "quant_act_static",
                  "norm": "rmsnorm_quant_act"}[args.act_scale]
 
     bf16_peak = float(peaks["bf16_tflops"])
-    if layer.codes == "bf16":
-        kern = "k_gemm_bf16c"
+    if layer.codes == "bf16" or layer.tokens > pipeline.I8_TENSOR_MIN_TOKENS:
+        if layer.codes == "bf16":
+            kern, what = "k_gemm_bf16c", "tcgen05 kind::f16 on bf16-coded int8"
+        else:
+            kern, what = "k_gemm_i8c", "int8 codes widened to fp16 on chip, tcgen05 kind::f16"
         roofline = {"bound": "tensor", "achieved": gemm_tops, "peak": bf16_peak, "unit": "TFLOP/s",
                     "frac": gemm_tops / bf16_peak,
                     "traffic": NCU_TRAFFIC_BYTES.get((kern, case.name)),
-                    "kernel": f"{kern} (sq_w8a8_gemm, tcgen05 kind::f16 on bf16-coded int8)",
-                    "peak_source": f"bf16 dense burst, {peaks_kind}"}
+                    "kernel": f"{kern} (sq_w8a8_gemm, {what})",
+                    "peak_source": f"bf16 dense burst, {peaks_kind} (fp16 runs at the same rate)"}
     else:
         kern = "k_gemm_i8_mma"
         gbs = nbytes["gemm"] / (float(gemm_ms.mean()) * 1e-3) / 1e9
@@ -368,11 +393,15 @@ def run_ours(args, case_name):
             layers = [layer, pipeline.Layer.for_case(case, codes=layer.codes)]
             line["e2e"] = run_e2e(layers, x_host, w_host, args.e2e_steps, ops, world, torch)
     if rank == 0 and not args.no_cpu_baseline:
-        times, o_ops = time_oracle(case, 20.0, min(case.tokens, 256), 3)
+        nt = min(case.tokens, 256)
+        times, o_ops, cores = time_oracle(case, 20.0, nt, 3)
+        t1, _, _ = time_oracle(case, 20.0, nt, 2, threads=1)
         line["cpu_baseline"] = {"value": o_ops * len(times) / sum(times) / 1e12, "unit": "TOPS",
-                                "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"whole path on the first {min(case.tokens, 256)} tokens with "
-                                          f"the full {case.cin}x{case.cout} weight, {len(times)} runs"}
+                                "cores": cores, "kind": "oracle",
+                                "value_one_thread": o_ops * len(t1) / sum(t1) / 1e12,
+                                "sample": f"whole path on the first {nt} tokens with the full "
+                                          f"{case.cin}x{case.cout} weight, {len(times)} runs on "
+                                          f"{cores} BLAS threads ({len(t1)} on one)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -316,8 +316,11 @@ sq_status sq_rotate_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin
  * k products of 127 * 127 could leave int32: SQ_ERR_UNSUPPORTED).
  * SQ_CODES_BF16 runs on the tcgen05 tensor
  * cores (fp32 accumulation in TMEM, converted to int32 every <= 1024
- * products so every partial sum stays an exact integer); SQ_CODES_I8 runs
- * on the legacy integer mma.sync path, which suits small m (decode).
+ * products so every partial sum stays an exact integer).  SQ_CODES_I8 reads
+ * one byte per code: m <= 16 runs the weight-streaming decode kernel
+ * (codes widened to fp16 on chip, mma.sync), 16 < m <= 64 the integer
+ * mma.sync kernel, m > 64 the tcgen05 tensor cores with the codes widened
+ * to fp16 in shared memory; every path accumulates exactly.
  * A pipeline wait that runs out sets SQ_FLAG_TIMEOUT.
  */
 #define SQ_GEMM_MAX_K 133136 /* largest multiple of 16 with k * 127^2 < 2^31 */
@@ -443,6 +446,31 @@ int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int6
  */
 sq_status sq_read_device_flags(int32_t* dev_flags, int clear, int32_t* flags_out,
                                cudaStream_t stream);
+
+/*
+ * Test hooks for the bounded waits.  No source page has a counterpart: they
+ * let a test drive the abort path of the kernels' pipelines on a GPU without
+ * faulting it.  Each call enqueues the same kernel as its product entry
+ * point, with its copy producer stalled (it issues no copies), so the first
+ * wait for a copy (or for work that depends on one) runs out after wait_ns
+ * nanoseconds; the kernel then sets SQ_FLAG_TIMEOUT in *dev_flags, stops,
+ * releases what it holds (tensor memory, barriers) and returns, leaving the
+ * device usable for the next call.  Outputs are unspecified.
+ *   sq_test_w8a8_gemm_stalled: the kernel sq_w8a8_gemm would run for these
+ *     arguments (SQ_ERR_UNSUPPORTED for the one GEMM kernel without pipeline
+ *     waits: 1-byte codes with 17 to 64 tokens).
+ *   sq_test_quant_act_stalled: the kernel of sq_quant_act.
+ * dev_flags is required; 1e5 <= wait_ns <= 1e9 (else SQ_ERR_INVALID_ARG).
+ * Other arguments as the product entry points.
+ */
+sq_status sq_test_w8a8_gemm_stalled(const void* xq, const float* x_scale, const void* wq,
+                                    const float* w_scale, sq_codes fmt, int64_t m, int64_t n,
+                                    int64_t k, void* y, int32_t* dev_flags, uint64_t wait_ns,
+                                    cudaStream_t stream);
+sq_status sq_test_quant_act_stalled(const void* x, sq_dtype dt, int64_t tokens, int64_t cin,
+                                    int64_t ldx, const float* s_inv, void* xq, sq_codes fmt,
+                                    float* x_scale, int32_t* dev_flags, uint64_t wait_ns,
+                                    cudaStream_t stream);
 
 /* Static text for a status code. */
 const char* sq_status_string(sq_status status);

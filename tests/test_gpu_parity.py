@@ -309,6 +309,12 @@ def test_gemm_saturated_widest_k(sq, codes):
     # 1024-product chunks
     (129, 72, 80), (520, 3080, 272), (777, 3464, 1040), (777, 4040, 2064), (2048, 2168, 208),
     (300, 1000, 3088),
+    # one-CTA tensor-core tiles (64 < M <= 128): K tail, several chunks
+    (65, 300, 2064), (100, 520, 1040), (128, 264, 64),
+    # weight-streaming decode kernel (M <= 16): one or two token tiles, a
+    # ragged channel block, K tails inside a stage and a k-block, more than
+    # 1024 products per warp (the fp32 -> int32 flush)
+    (8, 4096, 4096), (16, 100, 2064), (3, 33, 16), (16, 4096, 11008), (9, 72, 560),
     # int8 codes: weight rows staged in shared memory up to K = 12288 (a
     # ragged last block of rows, M in each of the 16/32/64-token tilings),
     # the register-fed kernel beyond it
@@ -324,6 +330,52 @@ def test_gemm_shapes_random_codes(sq, codes, m, n, k):
     assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref_acc)
     assert O.bf16_ulp_distance(y_bits(y), ref_y).max() <= 1
 
+
+
+def carrier_adversarial_codes(m, n, k, seed):
+    """Codes built against the fp32 carrier of the tensor-core GEMM.
+
+    Within each group of 16 products (one MMA's K) fifteen are +-127 * 127
+    and one is +-1, so every 1024-product chunk sums to within 2^20 of its
+    largest possible magnitude 1024 * 127^2 (just under 2^24) while carrying
+    unit terms an adder keeping fewer than 24 bits would drop; the sign of
+    whole chunks flips at chunk edges (rows by one pattern, columns by
+    another), the odd position of the unit term moves from group to group,
+    and a share of rows and columns alternates sign product by product."""
+    rng = np.random.default_rng(seed)
+    kk = np.arange(k)
+    unit_pos = (kk // 16 * 7) % 16 == kk % 16            # one position per group of 16
+    a = np.where(unit_pos, 1, 127)[None, :] * np.ones((m, 1), np.int64)
+    b = np.where(unit_pos, 1, 127)[None, :] * np.ones((n, 1), np.int64)
+    chunk = kk // 1024
+    a *= np.where((chunk[None, :] + np.arange(m)[:, None]) % 2 == 0, 1, -1)   # row chunk signs
+    b *= np.where((chunk[None, :] * (np.arange(n)[:, None] % 3)) % 2 == 0, 1, -1)
+    unit_sign = rng.choice([-1, 1], size=(m, k))
+    a = np.where(unit_pos[None, :], a * unit_sign, a)
+    alt = rng.random(m) < 0.25                             # rows alternating product by product
+    a[alt] *= np.where(kk % 2 == 0, 1, -1)[None, :]
+    altb = rng.random(n) < 0.25
+    b[altb] *= np.where(kk % 3 == 0, -1, 1)[None, :]
+    return a.astype(np.int8), b.astype(np.int8)
+
+
+@pytest.mark.parametrize("codes", gemm_code_formats())
+@pytest.mark.parametrize("m,n,k", [(256, 256, 2048 + 64), (100, 264, 3072), (300, 240, 1040),
+                                   (16, 256, 16384 + 64), (7, 40, 2048)])
+def test_gemm_fp32_carrier_adversarial(sq, codes, m, n, k):
+    """Exact accumulators on codes built against the fp32 carrier (chunk sums
+    near 2^24 with unit products in every MMA group, sign flips at chunk
+    edges)."""
+    xq, wq = carrier_adversarial_codes(m, n, k, seed=m + n + k)
+    ref_acc = O.int_accumulate(xq, wq)
+    chunk_max = np.abs(xq[:, :1024].astype(np.int64) @ wq[:, :1024].astype(np.int64).T).max()
+    assert chunk_max > 15 * 127 * 127 * 64 - 64 * 1 and chunk_max < 2 ** 24
+    xs = np.full(m, 1e-3, F32)
+    ws = np.full(n, 1e-4, F32)
+    y, acc = gemm_codes(sq, xq, xs, wq, ws, codes)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref_acc)
+    _, ref_y = O.w8a8_gemm(xq, xs, wq, ws)
+    assert O.bf16_ulp_distance(y_bits(y), ref_y).max() <= 1
 
 
 # ------------------------------------------------------------------ launch-shape coverage
@@ -406,15 +458,22 @@ FULL = synth.WORKLOAD_ORDER[1:]
 
 
 def sample_rows(case, k=48):
+    """Every token for layers of up to 2048 tokens (the oracle's float64 BLAS
+    forms those accumulators in seconds); otherwise k spread tokens plus
+    every massive-outlier token."""
+    if case.tokens <= 2048:
+        return np.arange(case.tokens)
     rows = set(np.linspace(0, case.tokens - 1, min(k, case.tokens)).astype(int).tolist())
-    # every massive-outlier token is sampled
     big = np.nonzero(np.abs(case.x_f32()).max(axis=1) >= 500)[0]
     rows.update(big.tolist())
     return np.array(sorted(rows))
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_workload_parity(sq, name):
+FULL_CODES = [(n, None) for n in FULL] + [(n, "i8") for n in FULL if synth.WORKLOADS[n]["tokens"] > 64]
+
+
+@pytest.mark.parametrize("name,codes", FULL_CODES, ids=[f"{n}-{c or 'auto'}" for n, c in FULL_CODES])
+def test_full_workload_parity(sq, name, codes):
     from w8a8_post_quantization_02_b300 import pipeline
     c = synth.workload(name)
     ref_ax = O.calibrate_absmax(c.x_f32(), 0)
@@ -425,7 +484,7 @@ def test_full_workload_parity(sq, name):
     rows = sample_rows(c)
     acc_ref, y_ref = O.w8a8_gemm(xq_ref, xs_ref, wq_ref, ws_ref, rows=rows)
 
-    layer = pipeline.Layer.for_case(c)
+    layer = pipeline.Layer.for_case(c, codes=codes)
     layer.load(dev(c.x, c.dtype), dev(c.w, c.dtype))
     layer.step(want_acc=True)
     torch.cuda.synchronize()

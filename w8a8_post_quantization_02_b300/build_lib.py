@@ -21,7 +21,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsq_b300.so")
 
 SOURCES = ["api.cu", "calib.cu", "smooth.cu", "act.cu", "act_static.cu", "weight.cu", "gemm_mma.cu",
-           "gemm_tc.cu", "noalloc.cu", "diag.cu", "rotate.cu"]
+           "gemm_tc.cu", "gemm_i8tc.cu", "gemm_dec.cu", "noalloc.cu", "diag.cu", "rotate.cu"]
 NO_FMAD = {"calib.cu", "smooth.cu", "act.cu", "act_static.cu", "weight.cu", "rotate.cu"}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-prec-div=true",

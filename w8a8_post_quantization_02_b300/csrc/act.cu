@@ -25,7 +25,7 @@ namespace sq {
 namespace {
 using namespace async;
 
-constexpr uint64_t kWaitNs = 1000000000ull;  // bound on every mbarrier wait (1 s)
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on every mbarrier wait of a product call (1 s)
 constexpr int kMaxStages = 8;
 
 template <bool BF16>
@@ -184,7 +184,8 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
                                                   uint8_t* __restrict__ xq,
                                                   float* __restrict__ x_scale, int32_t* flags,
                                                   int stages, const float* __restrict__ d_static,
-                                                  uint32_t* clipped, float eps) {
+                                                  uint32_t* clipped, float eps, uint64_t wait_ns,
+                                                  int stall) {
   constexpr bool STATIC = MODE == kStatic;
   constexpr bool NORM = MODE == kNorm;
   constexpr int E = BF16 ? 8 : 4;
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
   }
   __syncthreads();
   const uint64_t pol = policy_evict_first();  // X is read once here
-  if (tid == 0) {
+  if (tid == 0 && !stall) {  // stall: no copies (the bounded waits' test; 0 on every product call)
     for (int i = 0; i < stages; ++i) {
       const int64_t r = blockIdx.x + (int64_t)i * gridDim.x;
       if (r >= tokens) break;
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
   for (int64_t r = blockIdx.x; r < tokens; r += gridDim.x, ++it) {
     const int stage = it % stages;
     const uint32_t parity = (uint32_t)(it / stages) & 1u;
-    const bool ok = mbar_wait_bounded(&full[stage], parity, kWaitNs);
+    const bool ok = mbar_wait_bounded(&full[stage], parity, wait_ns);
     const uint8_t* buf = smem + (size_t)stage * row_bytes;
 
     // pass 1: X' = X * s^-1 into registers, and the thread's max|X'|
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
   if (aborted && tid == 0) {
     raise_flag(flags, SQ_FLAG_TIMEOUT);
     // let every copy this CTA issued land before its shared memory is freed
-    for (int k = 0; k < stages; ++k) {
+    for (int k = 0; k < stages && !stall; ++k) {
       const int j = it + k;
       if (blockIdx.x + (int64_t)j * gridDim.x >= tokens) break;
       mbar_wait_bounded(&full[j % stages], (uint32_t)(j / stages) & 1u, 10000000ull);
@@ -483,6 +484,8 @@ struct Static {
   const float* d;      // kStatic: the calibrated scale
   uint32_t* clipped;   // kStatic: clip counter or null
   float eps;           // kNorm
+  uint64_t wait_ns = kWaitNs;  // bound on each wait for a row's copy
+  int stall = 0;               // 1: no copies are issued (the bounded waits' test)
 };
 
 template <bool BF16, int CODES, int NT, int VPT, int MODE>
@@ -509,7 +512,7 @@ sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_byt
   occ = std::max(1, std::min(occ, 4));
   const int64_t grid = std::min<int64_t>(tokens, (int64_t)sm_count() * occ);
   kern<<<(unsigned)grid, NT, smem, st>>>(x, tokens, nvec, ldx_bytes, s_inv, xq, x_scale, flags,
-                                         stages, sc.d, sc.clipped, sc.eps);
+                                         stages, sc.d, sc.clipped, sc.eps, sc.wait_ns, sc.stall);
   return launch_status();
 }
 
@@ -579,6 +582,13 @@ sq_status quant_act(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int
                     const float* s_inv, void* xq, sq_codes fmt, float* x_scale, int32_t* flags,
                     cudaStream_t st) {
   return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags, Static{kDynamic, nullptr, nullptr, 0.0f}, st);
+}
+
+sq_status quant_act_stalled(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,
+                            const float* s_inv, void* xq, sq_codes fmt, float* x_scale, int32_t* flags,
+                            uint64_t wait_ns, cudaStream_t st) {
+  return quant_act_any(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, flags,
+                       Static{kDynamic, nullptr, nullptr, 0.0f, wait_ns, 1}, st);
 }
 
 sq_status quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_t cin, int64_t ldx,

@@ -35,7 +35,19 @@ int calibrate_kernel_count(sq_dtype, int64_t, int64_t, int64_t, int, int);
 sq_status gemm_i8_mma(const int8_t*, const float*, const int8_t*, const float*, int64_t, int64_t,
                       int64_t, void*, int32_t*, cudaStream_t);
 sq_status gemm_bf16c_tc(const void*, const float*, const void*, const float*, int64_t, int64_t,
-                        int64_t, void*, int32_t*, int32_t*, cudaStream_t);
+                        int64_t, void*, int32_t*, int32_t*, uint64_t, int, cudaStream_t);
+sq_status gemm_i8c_tc(const void*, const float*, const void*, const float*, int64_t, int64_t,
+                      int64_t, void*, int32_t*, int32_t*, uint64_t, int, cudaStream_t);
+sq_status quant_act_stalled(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, void*,
+                            sq_codes, float*, int32_t*, uint64_t, cudaStream_t);
+// Bound on each pipeline wait of the GEMM kernels in a product call.
+constexpr uint64_t kGemmWaitNs = 2000000000ull;
+sq_status gemm_dec(const int8_t*, const float*, const int8_t*, const float*, int64_t, int64_t, int64_t,
+                   void*, int32_t*, int32_t*, uint64_t, int, cudaStream_t);
+int64_t gemm_dec_max_m();
+// Token count above which 1-byte codes run on the tensor cores (below it
+// the weight-streaming kernels, whose grids cover the SMs at small M).
+constexpr int64_t kI8TensorCoreMinM = 64;
 
 namespace {
 bool valid_dtype(sq_dtype d) { return d == SQ_F32 || d == SQ_BF16; }
@@ -277,23 +289,64 @@ sq_status sq_channel_stats(const float* amax, const float* scale, int64_t n, dou
   return channel_stats(amax, scale, n, out, stream);
 }
 
+namespace {
+// The GEMM dispatch shared by sq_w8a8_gemm and its stalled test form.
+sq_status w8a8_gemm_dispatch(const void* xq, const float* x_scale, const void* wq,
+                             const float* w_scale, sq_codes fmt, int64_t m, int64_t n, int64_t k,
+                             void* y, int32_t* acc_out, int32_t* dev_flags, uint64_t wait_ns,
+                             int stall, cudaStream_t stream) {
+  if (!xq || !x_scale || !wq || !w_scale || !y || !valid_codes(fmt) || m < 1 || n < 1 || k < 16 ||
+      k % 16 != 0)
+    return SQ_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(y) & 3) ||
+      (reinterpret_cast<uintptr_t>(acc_out) & 3))
+    return SQ_ERR_INVALID_ARG;
+  if (k > SQ_GEMM_MAX_K) return SQ_ERR_UNSUPPORTED;  // int32 accumulators could wrap
+  if (fmt == SQ_CODES_I8 && m <= gemm_dec_max_m())
+    return gemm_dec(static_cast<const int8_t*>(xq), x_scale, static_cast<const int8_t*>(wq), w_scale,
+                    m, n, k, y, acc_out, dev_flags, wait_ns, stall, stream);
+  if (fmt == SQ_CODES_I8 && m <= kI8TensorCoreMinM) {
+    if (stall) return SQ_ERR_UNSUPPORTED;  // the mma.sync kernel has no pipeline waits
+    return gemm_i8_mma(static_cast<const int8_t*>(xq), x_scale, static_cast<const int8_t*>(wq),
+                       w_scale, m, n, k, y, acc_out, stream);
+  }
+  if (fmt == SQ_CODES_I8)
+    return gemm_i8c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, wait_ns, stall, stream);
+  return gemm_bf16c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, wait_ns, stall, stream);
+}
+}  // namespace
+
 sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
                        sq_codes fmt, int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out,
                        int32_t* dev_flags, void* workspace, size_t ws_bytes,
                        cudaStream_t stream) {
   (void)workspace;
   (void)ws_bytes;
-  if (!xq || !x_scale || !wq || !w_scale || !y || !valid_codes(fmt) || m < 1 || n < 1 || k < 16 ||
-      k % 16 != 0)
+  return w8a8_gemm_dispatch(xq, x_scale, wq, w_scale, fmt, m, n, k, y, acc_out, dev_flags, kGemmWaitNs,
+                            0, stream);
+}
+
+sq_status sq_test_w8a8_gemm_stalled(const void* xq, const float* x_scale, const void* wq,
+                                    const float* w_scale, sq_codes fmt, int64_t m, int64_t n,
+                                    int64_t k, void* y, int32_t* dev_flags, uint64_t wait_ns,
+                                    cudaStream_t stream) {
+  if (!dev_flags || wait_ns < 100000ull || wait_ns > 1000000000ull) return SQ_ERR_INVALID_ARG;
+  return w8a8_gemm_dispatch(xq, x_scale, wq, w_scale, fmt, m, n, k, y, nullptr, dev_flags, wait_ns, 1,
+                            stream);
+}
+
+sq_status sq_test_quant_act_stalled(const void* x, sq_dtype dt, int64_t tokens, int64_t cin,
+                                    int64_t ldx, const float* s_inv, void* xq, sq_codes fmt,
+                                    float* x_scale, int32_t* dev_flags, uint64_t wait_ns,
+                                    cudaStream_t stream) {
+  if (!dev_flags || wait_ns < 100000ull || wait_ns > 1000000000ull) return SQ_ERR_INVALID_ARG;
+  if (!x || !s_inv || !xq || !x_scale || !valid_dtype(dt) || !valid_codes(fmt) || tokens < 1 ||
+      cin < 1 || ldx < cin || cin % 16 != 0)
     return SQ_ERR_INVALID_ARG;
-  if (k > SQ_GEMM_MAX_K) return SQ_ERR_UNSUPPORTED;  // int32 accumulators could wrap
-  if (!aligned16(xq) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(y) & 3) ||
-      (reinterpret_cast<uintptr_t>(acc_out) & 3))
+  if (!aligned16(x) || (ldx * elem_bytes(dt)) % 16 != 0 || !aligned16(xq) || !aligned16(s_inv))
     return SQ_ERR_INVALID_ARG;
-  if (fmt == SQ_CODES_I8)
-    return gemm_i8_mma(static_cast<const int8_t*>(xq), x_scale, static_cast<const int8_t*>(wq),
-                       w_scale, m, n, k, y, acc_out, stream);
-  return gemm_bf16c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, stream);
+  if (cin > quant_act_max_cin(dt)) return SQ_ERR_UNSUPPORTED;
+  return quant_act_stalled(x, dt, tokens, cin, ldx, s_inv, xq, fmt, x_scale, dev_flags, wait_ns, stream);
 }
 
 sq_status sq_linear_host(const void* x_host, const void* w_host, sq_dtype dt, int64_t tokens,

@@ -29,15 +29,10 @@
 // the last wave of tiles.  Every mbarrier wait is bounded in time; a wait that runs out
 // sets SQ_FLAG_TIMEOUT, stops the CTA's loops, waits (bounded) for its own
 // outstanding copies and MMAs, frees TMEM and returns.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cudaTypedefs.h>
-
-#include "sq_async.cuh"
+#include "sq_tc.cuh"
 
 namespace sq {
 namespace tc {
-using async::su32;
 
 constexpr int BM = 128;       // accumulator lanes (rows of A) per CTA
 constexpr int BK = 64;        // 64 bf16 = one 128-byte swizzle row along K
@@ -47,7 +42,6 @@ constexpr int EPI_WARPS = 8;
 constexpr int THREADS = (2 + EPI_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;    // two accumulator buffers at columns 0 and 256
 constexpr uint32_t TMEM_BUF_STRIDE = 256;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
 template <int CG, int BN>
 struct Cfg {
@@ -80,155 +74,12 @@ struct Smem {
   int abort;
 };
 
-// ------------------------------------------------------------------ PTX wrappers
-SQ_DEVINL void mbar_init(uint64_t* b, uint32_t count) { async::mbar_init(b, count); }
-SQ_DEVINL void mbar_expect_tx(uint64_t* b, uint32_t bytes) { async::mbar_expect_tx(b, bytes); }
-SQ_DEVINL bool mbar_try_wait(uint64_t* b, uint32_t parity) { return async::mbar_try_wait(b, parity); }
-SQ_DEVINL uint64_t global_ns() { return async::global_ns(); }
-
-// Arrive on an mbarrier given by its shared::cluster address (this CTA's
-// or the peer's).  The barriers this is used on order tensor-memory reads
-// (completed by tcgen05.wait::ld, fenced by tcgen05.fence around the
-// arrive/wait pair) before the MMAs that overwrite the same columns; no
-// generic-memory data passes through them, so the default CTA-scope release
-// is enough (a cluster-scope release costs a memory barrier per arrive).
-SQ_DEVINL void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-
-// Bounded wait for the phase with parity `parity` to complete.  Returns
-// false if the CTA is aborting or the wait ran out (which starts the abort).
-SQ_DEVINL bool mbar_wait(uint64_t* b, uint32_t parity, int* abort_flag, int32_t* flags,
-                         uint64_t limit_ns = WAIT_LIMIT_NS) {
-  if (mbar_try_wait(b, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(b, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*(volatile int*)abort_flag) return false;
-      if (global_ns() - t0 > limit_ns) {
-        *(volatile int*)abort_flag = 1;
-        raise_flag(flags, SQ_FLAG_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// TMA load of box (x, y) into this CTA's shared memory, completing on the
-// mbarrier at shared::cluster address `bar` (with CG = 2, the even CTA's
-// barrier, which counts both CTAs' bytes).
-template <int CG>
-SQ_DEVINL void tma_load(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
-  if constexpr (CG == 2) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-  } else {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-        "[%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-  }
-}
-
-SQ_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-SQ_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor for a K-major tile stored as 128-byte rows
-// with the 128-byte swizzle (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
-// start address >> 4 in bits 0-13, leading byte offset (unused by this
-// layout) 16 >> 4 in bits 16-29, stride byte offset between 8-row groups
-// 1024 >> 4 in bits 32-45, the fixed value 1 in bits 46-48, base offset 0,
-// and swizzle mode 2 (128 B) in bits 61-63.
-SQ_DEVINL uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-template <int CG>
-SQ_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                        uint32_t accumulate) {
-  if constexpr (CG == 2) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-// Arrive (once) on `bar` when every MMA this thread issued so far has
-// completed; with CG = 2 on the barrier at the same offset in both CTAs.
-template <int CG>
-SQ_DEVINL void mma_commit(uint64_t* bar) {
-  if constexpr (CG == 2) {
-    const uint16_t mask = 3;
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-        "[%0], %1;" ::"r"(su32(bar)),
-        "h"(mask)
-        : "memory");
-  } else {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     su32(bar))
-                 : "memory");
-  }
-}
-
-template <int CG>
-SQ_DEVINL void tmem_alloc(uint32_t* dst) {
-  if constexpr (CG == 2) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(dst)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-  } else {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(dst)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-}
-
-template <int CG>
-SQ_DEVINL void tmem_dealloc(uint32_t taddr) {
-  if constexpr (CG == 2)
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS)
-                 : "memory");
-  else
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS)
-                 : "memory");
-}
-
-// 8 consecutive fp32 accumulator columns of this warp's 32 lanes.
-SQ_DEVINL void tmem_ld8(uint32_t taddr, uint32_t* r) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                 "=r"(r[7])
-               : "r"(taddr));
-}
-SQ_DEVINL void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-SQ_DEVINL int32_t f32_to_i32_exact(uint32_t bits) {
-  int32_t v;
-  asm("cvt.rni.s32.f32 %0, %1;" : "=r"(v) : "f"(__uint_as_float(bits)));
-  return v;
-}
-
 struct Problem {
   int64_t M, N, K;
   int tiles_m, tiles_n, n_kb, n_chunks;
   int vec_ok;  // N % 8 == 0 and y / acc_out 16-byte aligned: 16-byte stores
+  int stall;   // the producer issues no copies (the bounded waits' test): 0 on every product call
+  uint64_t wait_ns;  // bound on every pipeline wait
 };
 
 // ------------------------------------------------------------------ kernel
@@ -263,7 +114,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     async::prefetch_tensormap(&map_a);
     async::prefetch_tensormap(&map_b);
   }
-  if (warp == 1) tmem_alloc<CG>(&sm.tmem_base);
+  if (warp == 1) tmem_alloc<CG, TMEM_COLS>(&sm.tmem_base);
   tc_fence_before();
   if constexpr (CG == 2) {
     async::cluster_arrive();  // barriers initialised in both CTAs before any remote use
@@ -279,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs load their own halves)
-    if (lane == 0) {
+    if (lane == 0 && !P.stall) {
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
@@ -288,7 +139,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int m0 = (tile % P.tiles_m) * C::MMA_M + (int)rank * BM;
         const int n0 = (tile / P.tiles_m) * BN + (int)rank * C::B_ROWS;
         for (int kb = 0; kb < P.n_kb; ++kb) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1, &sm.abort, flags)) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1, &sm.abort, flags, P.wait_ns)) {
             ok = false;
             break;
           }
@@ -334,7 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = unit; ok && tile < num_tiles; tile += n_units) {
         for (int c = 0; ok && c < P.n_chunks; ++c) {
           const uint32_t buf = chunk_ctr & 1, use = chunk_ctr >> 1;
-          if (!mbar_wait(&sm.acc_empty[buf], (use & 1) ^ 1, &sm.abort, flags)) {
+          if (!mbar_wait(&sm.acc_empty[buf], (use & 1) ^ 1, &sm.abort, flags, P.wait_ns)) {
             ok = false;
             break;
           }
@@ -342,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t d = tmem + buf * TMEM_BUF_STRIDE;
           const int kb0 = c * CHUNK_KB, kb1 = min(P.n_kb, kb0 + CHUNK_KB);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&sm.full[stage], phase, &sm.abort, flags)) {
+            if (!mbar_wait(&sm.full[stage], phase, &sm.abort, flags, P.wait_ns)) {
               ok = false;
               break;
             }
@@ -350,7 +201,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t a_addr = su32(sm.a[stage]), b_addr = su32(sm.b[stage]);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16<CG>(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), C::IDESC,
+              mma_f16<CG>(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), C::IDESC,
                            (kb > kb0 || kk > 0) ? 1u : 0u);
             mma_commit<CG>(&sm.empty[stage]);
             if (++stage == C::STAGES) {
@@ -390,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // one lane waits and the warp follows its result, so the warp stays
         // converged for the .sync.aligned TMEM loads
         int got = 1;
-        if (lane == 0) got = mbar_wait(&sm.acc_full[buf], use & 1, &sm.abort, flags) ? 1 : 0;
+        if (lane == 0) got = mbar_wait(&sm.acc_full[buf], use & 1, &sm.abort, flags, P.wait_ns) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
         if (!got) {
           ok = false;
@@ -481,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc<CG>(tmem);
+    tmem_dealloc<CG, TMEM_COLS>(tmem);
   }
 }
 
@@ -503,7 +354,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint3
 template <int CG, int BN>
 sq_status launch(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
                  int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
-                 cudaStream_t st) {
+                 uint64_t wait_ns, int stall, cudaStream_t st) {
   using C = Cfg<CG, BN>;
   CUtensorMap ma, mb;
   if (!make_map(&ma, xq, m, k, BM) || !make_map(&mb, wq, n, k, C::B_ROWS)) return SQ_ERR_CUDA;
@@ -523,6 +374,8 @@ sq_status launch(const void* xq, const float* x_scale, const void* wq, const flo
   P.n_kb = (int)((k + BK - 1) / BK);
   P.n_chunks = (P.n_kb + CHUNK_KB - 1) / CHUNK_KB;
   P.vec_ok = (n % 8 == 0) && aligned16(y) && (acc_out == nullptr || aligned16(acc_out));
+  P.stall = stall;
+  P.wait_ns = wait_ns;
   const int tiles = P.tiles_m * P.tiles_n;
   const int units = std::min(tiles, sm_count() / CG);
   cudaLaunchConfig_t cfg = {};
@@ -561,19 +414,22 @@ int choose_bn(int64_t m, int64_t n, int units, int mma_m) {
 
 }  // namespace tc
 
+// The CTA-pair output-channel tile (256 or 240) for an M x N problem.
+int choose_bn_pair(int64_t m, int64_t n, int units, int mma_m) { return tc::choose_bn(m, n, units, mma_m); }
+
 // Tiles of 256 rows (CTA pairs) once M exceeds one 128-row tile.
 int gemm_bf16c_cta_group(int64_t m) { return m > tc::BM ? 2 : 1; }
 
 sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
                         int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
-                        cudaStream_t st) {
+                        uint64_t wait_ns, int stall, cudaStream_t st) {
   using namespace tc;
   if (m > (int64_t)1 << 31 || n > (int64_t)1 << 31 || k > (int64_t)1 << 31) return SQ_ERR_UNSUPPORTED;
   if (gemm_bf16c_cta_group(m) == 1)
-    return launch<1, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+    return launch<1, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
   if (choose_bn(m, n, sm_count() / 2, 2 * BM) == 240)
-    return launch<2, 240>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
-  return launch<2, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, st);
+    return launch<2, 240>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
+  return launch<2, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
 }
 
 }  // namespace sq

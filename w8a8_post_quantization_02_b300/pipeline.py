@@ -17,6 +17,9 @@ from . import sq
 # Token count from which the bf16-coded tensor-core GEMM is used; below it
 # the step streams int8 weight codes through the integer mma.sync path.
 TENSOR_PATH_MIN_TOKENS = 64
+# Above this token count the library runs 1-byte codes on the tensor cores
+# (the int8-operand tcgen05 kernel), at or below it on mma.sync.
+I8_TENSOR_MIN_TOKENS = 64
 
 
 def choose_codes(tokens: int) -> str:
@@ -74,10 +77,19 @@ class Layer:
         self.w.copy_(w)
 
     # bytes one step moves through HBM by definition of each step (the
-    # algorithmic traffic used for the roofline figures)
+    # algorithmic traffic used for the roofline figures): every INT8 code
+    # counts one byte, whatever format stores it
     def algorithmic_bytes(self) -> dict:
+        return self._bytes(code_bytes=1)
+
+    # bytes each step moves with the codes in their storage format (two bytes
+    # per code when they are stored as bf16 values)
+    def storage_bytes(self) -> dict:
+        return self._bytes(code_bytes=2 if self.codes == "bf16" else 1)
+
+    def _bytes(self, code_bytes: int) -> dict:
         eb = 2 if self.dtype == "bf16" else 4
-        cb = 2 if self.codes == "bf16" else 1
+        cb = code_bytes
         T, K, N = self.tokens, self.cin, self.cout
         return {
             "calibrate_x": T * K * eb + K * 4,
