@@ -412,8 +412,15 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
       if (v >= nvec) continue;
       float q[E];
       if (no_clamp) {
+        // two quotients per instruction, then the rounding add
 #pragma unroll
-        for (int e = 0; e < E; ++e) q[e] = magic_of(quot_rn(p[i][e], d, inv));
+        for (int e = 0; e < E; e += 2) {
+          float a = p[i][e], b = p[i][e + 1];
+          quot2_rn(a, b, d, d, inv, inv);
+          add2_rn(a, b, kMagic, kMagic);
+          q[e] = a;
+          q[e + 1] = b;
+        }
       } else if constexpr (STATIC) {
         // the quotient (quot_rn inside its range, else an IEEE division),
         // clamp, then the rounding add.  A NaN gives code 0 and +-inf

@@ -32,13 +32,16 @@
 //     BN/2 rows of B, and both CTAs' converter warps arrive on the even
 //     CTA's stage barrier before the even CTA's MMAs read the pair's shared
 //     memory.  Each converter thread first makes its shared-memory writes
-//     visible to the async proxy (fence.proxy.async) and the warp's arrive
-//     releases them: the writes are performed in the writer's own shared
-//     memory before the arrive leaves the SM, and the MMAs that read them are
-//     issued only after the arrive is observed.  The arrive and the wait use
-//     the default CTA-scope semantics, like the cluster barriers of the pair's
-//     other hand-offs; a cluster-scope release and acquire on every k-block
-//     measured 25-50 % slower on this kernel.
+//     visible to the async proxy (fence.proxy.async); the warp's arrive then
+//     releases them at CTA scope: in the even CTA on the stage barrier the
+//     MMA issuer waits on, in the odd CTA on a barrier of its own, whose
+//     completion one forwarder thread acquires and passes on to the even
+//     CTA with a single release at cluster scope per stage.  (With a
+//     CTA-scope release there, a stress test found whole rows of the odd
+//     CTA's tile read stale in 2 of 300 runs; with every converter warp
+//     releasing at cluster scope the kernel ran 75 % slower.)  The MMA
+//     issuer's wait keeps the CTA-scope acquire: acquiring at cluster scope
+//     on every k-block measured 25-90 % slower.
 // Every mbarrier wait is bounded in time; a wait that runs out sets
 // SQ_FLAG_TIMEOUT, stops the CTA's loops, waits (bounded) for its own
 // outstanding copies and MMAs, frees TMEM and returns.
@@ -58,6 +61,10 @@ constexpr int BM = 128;       // accumulator lanes (rows of A) per CTA
 constexpr int BK = 64;        // codes per k-block: a 64-byte int8 row, a 128-byte fp16 row
 constexpr int CHUNK_KB = 16;  // k-blocks per exact fp32 chunk (1024 products)
 constexpr int CONV_WARPS = 10;              // warps 2-11
+#ifndef SQ_I8C_PAIR
+#define SQ_I8C_PAIR 1
+#endif
+constexpr int PAIR = SQ_I8C_PAIR;            // k-blocks a converter warp loads before storing
 constexpr int EPI_WARPS = 8;                // warps 12-19
 constexpr int EPI_FIRST = 2 + CONV_WARPS;
 constexpr int THREADS = (2 + CONV_WARPS + EPI_WARPS) * 32;
@@ -110,7 +117,8 @@ struct Smem {
   uint8_t i8[C::S8][C::A8 + C::B8];
   uint64_t full8[C::S8];
   uint64_t empty8[C::S8];
-  uint64_t full16[C::S16];  // (even CTA) both CTAs' converters finished the stage
+  uint64_t full16[C::S16];     // (even CTA) both CTAs' converters finished the stage
+  uint64_t conv_done[C::S16];  // (odd CTA) its converters finished the stage
   uint64_t empty16[C::S16];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
@@ -182,16 +190,34 @@ SQ_DEVINL ConvOffsets conv_offsets(int wt) {
 }
 
 template <int VECS, int NW>
-SQ_DEVINL void convert_block(const uint8_t* src_stage, uint8_t* dst_stage, const ConvOffsets& o, int wt) {
-  static_assert(NW % 32 == 0, "NW / 4 rows keep the row within its swizzle atom");
+struct ConvRegs {
+  static constexpr int N = (VECS + NW - 1) / NW;  // vectors per thread per k-block
+  uint4 v[N];
+};
+
+// Load this thread's vectors of the int8 stage (the stage may be refilled
+// as soon as every converter has loaded it).
+template <int VECS, int NW>
+SQ_DEVINL void load_block(const uint8_t* src_stage, const ConvOffsets& o, int wt, ConvRegs<VECS, NW>& r) {
   const uint8_t* src = src_stage + o.src;
+#pragma unroll
+  for (int i = 0; i < ConvRegs<VECS, NW>::N; ++i) {
+    if (VECS % NW != 0 && i == VECS / NW && wt >= VECS % NW) break;
+    r.v[i] = *reinterpret_cast<const uint4*>(src + 16 * NW * i);
+  }
+}
+
+// Widen the loaded vectors into the fp16 stage.
+template <int VECS, int NW>
+SQ_DEVINL void store_block(uint8_t* dst_stage, const ConvOffsets& o, int wt, const ConvRegs<VECS, NW>& r) {
+  static_assert(NW % 32 == 0, "NW / 4 rows keep the row within its swizzle atom");
   uint8_t* d0 = dst_stage + o.dst0;
   uint8_t* d1 = dst_stage + o.dst1;
 #pragma unroll
-  for (int i = 0; i < (VECS + NW - 1) / NW; ++i) {
+  for (int i = 0; i < ConvRegs<VECS, NW>::N; ++i) {
     if (VECS % NW != 0 && i == VECS / NW && wt >= VECS % NW) break;
     uint4 lo, hi;
-    codes_to_f16(*reinterpret_cast<const uint4*>(src + 16 * NW * i), lo, hi);
+    codes_to_f16(r.v[i], lo, hi);
     *reinterpret_cast<uint4*>(d0 + 32 * NW * i) = lo;
     *reinterpret_cast<uint4*>(d1 + 32 * NW * i) = hi;
   }
@@ -221,7 +247,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&sm.empty8[s], CONV_WARPS);
     }
     for (int t = 0; t < C::S16; ++t) {
-      mbar_init(&sm.full16[t], CONV_WARPS * CG);
+      mbar_init(&sm.full16[t], CG == 2 ? CONV_WARPS + 1 : CONV_WARPS);  // + the odd CTA's forwarder
+      mbar_init(&sm.conv_done[t], CONV_WARPS);
       mbar_init(&sm.empty16[t], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -331,30 +358,69 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(&sm.drain, 0) && global_ns() - t0 < WAIT_LIMIT_NS) {
       }
+    } else if (CG == 2 && !leader && lane == 0) {
+      // odd CTA's forwarder: once this CTA's converters have finished a
+      // stage (acquired through conv_done), one arrive on the even CTA's
+      // stage barrier with release at cluster scope, cumulative over those
+      // writes, so they are performed for the even CTA's MMAs before the
+      // arrive reaches it (the converters themselves never wait on it)
+      for (int64_t g = 0; g < total_blocks; ++g) {
+        const int t = (int)(g % C::S16);
+        if (!mbar_wait(&sm.conv_done[t], (uint32_t)(g / C::S16) & 1u, &sm.abort, flags, P.wait_ns)) break;
+        mbar_arrive_release_cluster(full16_0 + t * 8);
+      }
     }
   } else {
     // ---------------- converters: every warp widens its share of every k-block
     const int wt = threadIdx.x - 64;  // 0 .. 32 * CONV_WARPS - 1
     const ConvOffsets off = conv_offsets(wt);
-    for (int64_t g = 0; g < total_blocks; ++g) {
-      const int s = (int)(g % C::S8), t = (int)(g % C::S16);
-      // one lane per warp polls the barriers; __syncwarp passes what it
-      // observed (the copies' completion, the MMAs' release of the stage)
-      // on to the other lanes
-      int ok_i = 1;
-      if (lane == 0) {
-        ok_i = mbar_wait(&sm.full8[s], (uint32_t)(g / C::S8) & 1u, &sm.abort, flags, P.wait_ns) &&
-               mbar_wait(&sm.empty16[t], ((uint32_t)(g / C::S16) & 1u) ^ 1u, &sm.abort, flags, P.wait_ns);
+    // PAIR k-blocks at a time: load them all (each int8 stage freed as soon
+    // as the warp holds its codes), then widen and store each once its fp16
+    // stage is free; the longer independent runs hide the loads' latency.
+    for (int64_t g0 = 0; g0 < total_blocks; g0 += PAIR) {
+      ConvRegs<C::VECS, CONV_WARPS * 32> regs[PAIR];
+      bool ok = true;
+#pragma unroll
+      for (int p = 0; p < PAIR; ++p) {
+        const int64_t g = g0 + p;
+        if (g >= total_blocks) break;
+        const int s = (int)(g % C::S8);
+        // one lane per warp polls the barrier; __syncwarp passes what it
+        // observed (the copies' completion) on to the other lanes
+        int ok_i = 1;
+        if (lane == 0) ok_i = mbar_wait(&sm.full8[s], (uint32_t)(g / C::S8) & 1u, &sm.abort, flags, P.wait_ns);
+        if (!__shfl_sync(0xFFFFFFFFu, ok_i, 0)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        load_block<C::VECS, CONV_WARPS * 32>(sm.i8[s], off, wt, regs[p]);
+        __syncwarp();
+        if (lane == 0) async::mbar_arrive_local(&sm.empty8[s]);
       }
-      if (!__shfl_sync(0xFFFFFFFFu, ok_i, 0)) break;
-      __syncwarp();
-      convert_block<C::VECS, CONV_WARPS * 32>(sm.i8[s], sm.f16[t], off, wt);
-      fence_proxy_async_smem();  // this thread's fp16 writes as the tensor cores will read them
-      __syncwarp();
-      if (lane == 0) {
-        async::mbar_arrive_local(&sm.empty8[s]);
-        mbar_arrive_cluster(full16_0 + t * 8);
+      if (!ok) break;
+#pragma unroll
+      for (int p = 0; p < PAIR; ++p) {
+        const int64_t g = g0 + p;
+        if (g >= total_blocks) break;
+        const int t = (int)(g % C::S16);
+        // the MMAs' release of the stage, passed on by __syncwarp
+        int ok_i = 1;
+        if (lane == 0)
+          ok_i = mbar_wait(&sm.empty16[t], ((uint32_t)(g / C::S16) & 1u) ^ 1u, &sm.abort, flags, P.wait_ns);
+        if (!__shfl_sync(0xFFFFFFFFu, ok_i, 0)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        store_block<C::VECS, CONV_WARPS * 32>(sm.f16[t], off, wt, regs[p]);
+        fence_proxy_async_smem();  // this thread's fp16 writes as the tensor cores will read them
+        __syncwarp();
+        // the even CTA's converters arrive on its stage barrier; the odd
+        // CTA's on their own CTA's barrier, which its forwarder passes on
+        if (lane == 0) async::mbar_arrive_local(leader ? &sm.full16[t] : &sm.conv_done[t]);
       }
+      if (!ok) break;
     }
   }
   } else {
@@ -538,20 +604,17 @@ sq_status launch(const void* xq, const float* x_scale, const void* wq, const flo
 
 }  // namespace tc8
 
-int choose_bn_pair(int64_t m, int64_t n, int units, int mma_m);  // gemm_tc.cu
-
-// 1-byte codes on the tensor cores: tiles of 256 rows (CTA pairs) once M
-// exceeds one 128-row tile; the output-channel tile as for the bf16-coded
-// path.
+// 1-byte codes on the tensor cores: one CTA per 128 x 256 tile.  The
+// CTA-pair form (CG = 2, kept above) measured slower on B300 (prefill layer
+// 262 us against 247 us): the odd CTA's widened tiles reach the even CTA's
+// MMAs only through a cluster-scope release per stage, whose latency the
+// rings do not hide.
 sq_status gemm_i8c_tc(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
                       int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
                       uint64_t wait_ns, int stall, cudaStream_t st) {
   using namespace tc8;
   if (m > (int64_t)1 << 31 || n > (int64_t)1 << 31 || k > (int64_t)1 << 31) return SQ_ERR_UNSUPPORTED;
-  if (m <= BM) return launch<1, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
-  if (choose_bn_pair(m, n, sm_count() / 2, 2 * BM) == 240)
-    return launch<2, 240>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
-  return launch<2, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
+  return launch<1, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
 }
 
 }  // namespace sq

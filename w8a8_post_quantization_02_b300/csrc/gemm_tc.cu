@@ -414,9 +414,6 @@ int choose_bn(int64_t m, int64_t n, int units, int mma_m) {
 
 }  // namespace tc
 
-// The CTA-pair output-channel tile (256 or 240) for an M x N problem.
-int choose_bn_pair(int64_t m, int64_t n, int units, int mma_m) { return tc::choose_bn(m, n, units, mma_m); }
-
 // Tiles of 256 rows (CTA pairs) once M exceeds one 128-row tile.
 int gemm_bf16c_cta_group(int64_t m) { return m > tc::BM ? 2 : 1; }
 

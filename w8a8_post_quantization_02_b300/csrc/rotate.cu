@@ -168,7 +168,13 @@ __global__ void __launch_bounds__(1024) k_rotate_rows(const uint8_t* __restrict_
       float c[E];
       if (fast) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) c[e] = magic_of(quot_rn(f[i][e], d, inv));
+        for (int e = 0; e < E; e += 2) {
+          float a = f[i][e], b = f[i][e + 1];
+          quot2_rn(a, b, d, d, inv, inv);
+          add2_rn(a, b, kMagic, kMagic);
+          c[e] = a;
+          c[e + 1] = b;
+        }
       } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) c[e] = code_div_magic(f[i][e], d, qmax);

@@ -145,6 +145,33 @@ SQ_DEVINL void add2_rn(float& a0, float& a1, float b0, float b1) {
       : "f"(b0), "f"(b1));
 }
 
+SQ_DEVINL void fma2_rn(float& a0, float& a1, float b0, float b1, float c0, float c1) {
+  // (a0, a1) = (RN(a0 * b0 + c0), RN(a1 * b1 + c1)), each one fused multiply-add
+  asm("{\n.reg .b64 x, y, z;\nmov.b64 x, {%0, %1};\nmov.b64 y, {%2, %3};\nmov.b64 z, {%4, %5};\n"
+      "fma.rn.f32x2 x, x, y, z;\nmov.b64 {%0, %1}, x;\n}\n"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Two quotients RN(v0 / d0), RN(v1 / d1) by quot_rn's sequence (sq_common.cuh:
+// y = RN(1/d), one multiply and four fused multiply-adds, Markstein's
+// correction), two lanes per instruction; the same preconditions.
+SQ_DEVINL void quot2_rn(float& v0, float& v1, float d0, float d1, float y0, float y1) {
+  float q0 = v0, q1 = v1;
+  mul2_rn(q0, q1, y0, y1);
+  float r0 = -d0, r1 = -d1;
+  fma2_rn(r0, r1, q0, q1, v0, v1);   // v - d q
+  fma2_rn(r0, r1, y0, y1, q0, q1);   // q + r y
+  q0 = r0;
+  q1 = r1;
+  r0 = -d0;
+  r1 = -d1;
+  fma2_rn(r0, r1, q0, q1, v0, v1);
+  fma2_rn(r0, r1, y0, y1, q0, q1);
+  v0 = r0;
+  v1 = r1;
+}
+
 // max(|m|, |v|) in magnitude, NaN if either is NaN; the sign of the result
 // is meaningless (callers take the magnitude at the end).
 SQ_DEVINL float absmax_nan(float m, float v) {

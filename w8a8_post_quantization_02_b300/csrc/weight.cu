@@ -403,7 +403,10 @@ __global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__
           for (int e = 0; e < EPC; e += 2) mul2_rn(q[k][e], q[k][e + 1], sj, sj);
           if (!clamp) {
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) q[k][e] = magic_of(quot_rn(q[k][e], dch[e], inv[e]));
+            for (int e = 0; e < EPC; e += 2) {
+              quot2_rn(q[k][e], q[k][e + 1], dch[e], dch[e + 1], inv[e], inv[e + 1]);
+              add2_rn(q[k][e], q[k][e + 1], kMagic, kMagic);
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < EPC; ++e) q[k][e] = code_div_magic(q[k][e], dch[e], 127.0f);
