@@ -157,12 +157,14 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- the oracle arm
 def blas_threads() -> int:
+    """BLAS threads of this process: threadpoolctl's count where it is
+    installed, else the OpenBLAS thread variable the parent set."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
         return max(n) if n else 1
-    except Exception:  # pragma: no cover
-        return 1
+    except ImportError:
+        return int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0) or host_cores()
 
 
 def oracle_sample_case(case, tokens: int):
@@ -179,29 +181,43 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def time_oracle(case, budget_s: float, sample_tokens: int, max_steps: int, threads: int | None = None):
-    """Run the oracle's whole path on a token sample of the layer (full W)
-    until ``max_steps`` runs or ``budget_s`` seconds are used, with the BLAS
-    library (the oracle's one multi-threaded primitive, the accumulator
-    matmul) limited to ``threads`` (default: every core this process may
-    use).  Returns (times, ops, threads used)."""
+def oracle_child(case_name: str, budget_s: float, sample_tokens: int, max_steps: int) -> dict:
+    """Body of the oracle timing process (see time_oracle)."""
     from oracle import sq_oracle as O
-    from threadpoolctl import threadpool_limits
-    n = threads or host_cores()
+    from w8a8_post_quantization_02_b300 import synth
+    case = synth.workload(case_name)
     sc = oracle_sample_case(case, sample_tokens)
     x, w = sc.x_f32(), sc.w_f32()
     times = []
-    with threadpool_limits(limits=n, user_api="blas"):
-        t_start = time.perf_counter()
-        while len(times) < max_steps:
-            t0 = time.perf_counter()
-            O.run_path(x, w, sc.alpha)
-            times.append(time.perf_counter() - t0)
-            if time.perf_counter() - t_start > budget_s:
-                break
-        used = blas_threads()
-    ops = 2 * sample_tokens * case.cin * case.cout
-    return times, ops, used
+    t_start = time.perf_counter()
+    while len(times) < max_steps:
+        t0 = time.perf_counter()
+        O.run_path(x, w, sc.alpha)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    return {"times": times, "ops": 2 * sample_tokens * case.cin * case.cout, "threads": blas_threads()}
+
+
+def time_oracle(case_name: str, budget_s: float, sample_tokens: int, max_steps: int,
+                threads: int | None = None):
+    """Run the oracle's whole path on a token sample of the layer (full W)
+    until ``max_steps`` runs or ``budget_s`` seconds are used, with the BLAS
+    library (the oracle's one multi-threaded primitive, the accumulator
+    matmul) on ``threads`` threads (default: every core this process may
+    use).  It runs in a fresh interpreter whose thread count is fixed by the
+    environment before numpy loads, so the limit holds without a runtime
+    thread-control package and the oracle never shares a process with CUDA.
+    Returns (times, ops, threads used)."""
+    n = str(threads or host_cores())
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=n, OMP_NUM_THREADS=n, MKL_NUM_THREADS=n)
+    code = ("import json, bench; print(json.dumps(bench.oracle_child(%r, %r, %d, %d)))"
+            % (case_name, float(budget_s), sample_tokens, max_steps))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing process failed:\n" + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["times"], d["ops"], d["threads"]
 
 
 def run_reference(args, case_name):
@@ -211,9 +227,9 @@ def run_reference(args, case_name):
         return 0
     case = synth.workload(case_name)
     sample_tokens = min(case.tokens, 256)
-    # warm-up runs (untimed), then the timed steps within a few minutes
-    time_oracle(case, 0.0, sample_tokens, max(1, min(args.warmup, 1)))
-    times, ops, cores = time_oracle(case, 150.0, sample_tokens, args.steps)
+    # one untimed run first (warm-up), then the timed steps within a few minutes
+    times, ops, cores = time_oracle(case_name, 150.0, sample_tokens, args.steps + 1)
+    times = times[1:] or times
     sec = sum(times)
     value = ops * len(times) / sec / 1e12
     line = {
@@ -250,10 +266,6 @@ def to_device(case, torch):
 # on the same workload (dram__bytes_read.sum + dram__bytes_write.sum), or
 # absent when the kernel changed after the capture.
 NCU_TRAFFIC_BYTES = {
-    # 109.38 MB read + 26.36 MB written (the rest of Y still dirty in L2)
-    ("k_gemm_bf16c", "prefill_upgate_2048x4096x11008"): 135.74e6,
-    # 16.88 MB read (the int8 weight codes and X codes), nothing written back yet
-    ("k_gemm_i8_mma", "decode_7b_16x4096x4096"): 16.88e6,
 }
 
 
@@ -367,11 +379,14 @@ def run_ours(args, case_name):
                     "kernel": f"{kern} (sq_w8a8_gemm, {what})",
                     "peak_source": f"bf16 dense burst, {peaks_kind} (fp16 runs at the same rate)"}
     else:
-        kern = "k_gemm_i8_mma"
+        if layer.tokens <= 16:
+            kern, what = "k_gemm_dec", "weight-streaming decode kernel, mma.sync f16 on widened codes"
+        else:
+            kern, what = "k_gemm_i8_mma", "mma.sync s8"
         gbs = nbytes["gemm"] / (float(gemm_ms.mean()) * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                     "traffic": NCU_TRAFFIC_BYTES.get((kern, case.name)),
-                    "kernel": f"{kern} (sq_w8a8_gemm, mma.sync s8)",
+                    "kernel": f"{kern} (sq_w8a8_gemm, {what})",
                     "peak_source": f"HBM copy, {peaks_kind}"}
     launches = layer.kernel_count() * K
     line = {
@@ -394,8 +409,8 @@ def run_ours(args, case_name):
             line["e2e"] = run_e2e(layers, x_host, w_host, args.e2e_steps, ops, world, torch)
     if rank == 0 and not args.no_cpu_baseline:
         nt = min(case.tokens, 256)
-        times, o_ops, cores = time_oracle(case, 20.0, nt, 3)
-        t1, _, _ = time_oracle(case, 20.0, nt, 2, threads=1)
+        times, o_ops, cores = time_oracle(case.name, 20.0, nt, 3)
+        t1, _, _ = time_oracle(case.name, 20.0, nt, 2, threads=1)
         line["cpu_baseline"] = {"value": o_ops * len(times) / sum(times) / 1e12, "unit": "TOPS",
                                 "cores": cores, "kind": "oracle",
                                 "value_one_thread": o_ops * len(t1) / sum(t1) / 1e12,

@@ -315,6 +315,8 @@ def test_gemm_saturated_widest_k(sq, codes):
     # ragged channel block, K tails inside a stage and a k-block, more than
     # 1024 products per warp (the fp32 -> int32 flush)
     (8, 4096, 4096), (16, 100, 2064), (3, 33, 16), (16, 4096, 11008), (9, 72, 560),
+    # more than 8192 codes of K per CTA: several exact fp32 chunks per CTA
+    (16, 24, 66048), (3, 200, 70000),
     # int8 codes: weight rows staged in shared memory up to K = 12288 (a
     # ragged last block of rows, M in each of the 16/32/64-token tilings),
     # the register-fed kernel beyond it

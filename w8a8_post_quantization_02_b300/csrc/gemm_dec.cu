@@ -5,24 +5,28 @@
 // bound by streaming the weights from memory; paragraph 2: both matmul
 // operands are INT8.
 //
-// A CTA owns 32 output channels.  Its 16 compute warps split K: warp w
-// owns codes [256 w, 256 w + 256) of every 4096-code chunk of K.  The MMA
-// is mma.sync m16n8k16 with the tokens as the M side (up to 16) and the
-// channels as the N side (four tiles of 8): a warp widens the tokens' codes
-// of its K range to exact fp16 fragments once and reuses them for all 32
-// channels, so each weight code is loaded and widened exactly once.  Warp
-// 0 issues, per chunk, every warp's 2-D TMA boxes (128 codes x 32 channel
-// rows and 128 codes x 16 token rows, 128-byte swizzle; rows past N or M
-// and codes past K arrive as 0) on that warp's own barrier, so each warp
-// starts as soon as its slice has landed.  Within a 128-code k-block, lane
-// c hands codes 32c + 4j .. 32c + 4j + 3 to k16 step j (j = 0..7); the MMA
-// reads them as k = 2c, 2c+1, 2c+8, 2c+9 on both operands, so every
-// product still pairs a token and a channel at the same k and the sum is
-// unchanged.  Products are exact in fp32 and each warp converts its sums to
-// int32 after every chunk (at most 256 products per output); the warps'
-// int32 sums meet in shared memory at the end and the epilogue writes Y
-// (and the accumulators).  Every mbarrier wait is bounded; one that runs
-// out sets SQ_FLAG_TIMEOUT.
+// A CTA owns 32 output channels and has 16 warps that split K: warp w
+// owns codes [256 w, 256 w + 256) of every 4096-code chunk of K, as two
+// 128-code k-blocks.  The MMA is mma.sync m16n8k16 with the tokens as the
+// M side (up to 16) and the channels as the N side (four tiles of 8): a
+// warp widens the tokens' codes of a k-block to exact fp16 fragments once
+// and reuses them for all 32 channels, so each weight code is loaded and
+// widened exactly once.  Each warp fetches its own k-blocks (one lane
+// issues, per k-block, a 2-D TMA box of 128 codes x 32 channel rows and one
+// of 128 codes x 16 token rows, 128-byte swizzle; rows past N or M and
+// codes past K arrive as 0) into two buffers with a barrier each, and
+// refetches a buffer for the next chunk as soon as it has consumed it.
+// Sixteen issuing warps instead of one producer thread: a single thread
+// issuing the CTA's 64 boxes took about 6 us on B300, longer than the
+// weights take to stream from HBM.  Within a k-block, lane c hands codes
+// 32c + 4j .. 32c + 4j + 3 to k16 step j (j = 0..7); the MMA reads them as
+// k = 2c, 2c+1, 2c+8, 2c+9 on both operands, so every product still pairs a
+// token and a channel at the same k and the sum is unchanged.  Products are
+// exact in fp32 and each warp converts its sums to int32 after every chunk
+// (at most 256 products per output); the warps' int32 sums meet in shared
+// memory at the end, and each thread writes one output of Y (and of the
+// accumulators) with the scales it loaded before the first copy landed.
+// Every mbarrier wait is bounded; one that runs out sets SQ_FLAG_TIMEOUT.
 #include <cuda_bf16.h>
 
 #include "sq_async.cuh"
@@ -33,13 +37,16 @@ using namespace async;
 
 constexpr int kChan = 32;                         // output channels per CTA (four n8 tiles)
 constexpr int kKBlock = 128;                      // codes per k-block (one swizzled 128-byte box row)
-constexpr int kWarps = 16;                        // compute warps, two k-blocks of every chunk each
+constexpr int kWarps = 16;                        // warps, two k-blocks of every chunk each
 constexpr int kChunk = 2 * kKBlock * kWarps;      // codes of K per chunk (4096)
-constexpr int kThreads = 32 * (1 + kWarps);
+constexpr int kThreads = 32 * kWarps;             // one output (token, channel) per thread at the end
 constexpr int kWBox = kChan * kKBlock;            // bytes of one channel box (4 KiB)
 constexpr int kXBox = 16 * kKBlock;               // bytes of one token box (2 KiB)
-constexpr int kSlice = 2 * (kWBox + kXBox);       // bytes of one warp's slice of a chunk
+constexpr int kBuf = kWBox + kXBox;               // one k-block buffer: channel box, then token box
+constexpr int kSlice = 2 * kBuf;                  // a warp's two buffers
 constexpr int kSmem = kWarps * kSlice + 2 * kWarps * 8 + 16 + 1024;
+static_assert(kThreads == 16 * kChan, "the epilogue maps threads onto 16 tokens x 32 channels");
+static_assert(kWBox % 1024 == 0 && kXBox % 1024 == 0, "boxes start on 128-byte-swizzle atoms");
 
 SQ_DEVINL uint32_t hsub2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -75,23 +82,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                int32_t* flags, uint64_t wait_ns, int stall) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWarps * kSlice);  // [warp]: its slice landed
-  uint64_t* empty = full + kWarps;                                       // [warp]: done with its slice
-  int* abort_flag = reinterpret_cast<int*>(empty + kWarps);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWarps * kSlice);  // [warp][buffer]
+  int* abort_flag = reinterpret_cast<int*>(full + 2 * kWarps);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n0 = (int64_t)blockIdx.x * kChan;
   const int nch = (int)(N - n0 < kChan ? N - n0 : kChan);
   const int64_t nchunks = (K + kChunk - 1) / kChunk;
 
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w) {
-      mbar_init(&full[w], 1);
-      mbar_init(&empty[w], 1);
-    }
+    for (int b = 0; b < 2 * kWarps; ++b) mbar_init(&full[b], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&map_w);
     prefetch_tensormap(&map_x);
+  }
+  // this thread's output at the end, and its two scales, loaded now so the
+  // loads overlap the weight stream
+  const int out_tk = threadIdx.x / kChan, out_ch = threadIdx.x % kChan;
+  const bool has_out = out_tk < M && out_ch < nch;
+  float xs = 0.0f, wsc = 0.0f;
+  if (has_out) {
+    xs = x_scale[out_tk];
+    wsc = w_scale[n0 + out_ch];
   }
   __syncthreads();
 
@@ -111,126 +123,120 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  if (warp == 0) {
-    // ---------------- producer: every warp's slice of every chunk, k-blocks below K only
-    // (stall: none, the bounded waits' test; 0 on every product call)
-    if (lane == 0 && !stall) {
-      int64_t issued_to = 0;  // chunks issued
-      bool ok = true;
-      for (int64_t ch = 0; ok && ch < nchunks; ++ch) {
-        for (int w = 0; w < kWarps; ++w) {
-          const int64_t k0 = ch * kChunk + (int64_t)w * 2 * kKBlock;
-          if (k0 >= K) break;  // this and later slices of the chunk lie past K
-          if (!wait(&empty[w], ((uint32_t)ch & 1u) ^ 1u)) {
-            ok = false;
-            break;
-          }
-          const int nb = K - k0 > kKBlock ? 2 : 1;
-          uint8_t* sl = smem + (size_t)w * kSlice;
-          mbar_expect_tx(&full[w], (uint32_t)nb * (kWBox + kXBox));
-          for (int b = 0; b < nb; ++b) {
-            tma_load_2d(sl + b * kWBox, &map_w, &full[w], (int)(k0 + b * kKBlock), (int)n0);
-            tma_load_2d(sl + 2 * kWBox + b * kXBox, &map_x, &full[w], (int)(k0 + b * kKBlock), 0);
-          }
-        }
-        if (ok) issued_to = ch + 1;
-      }
-      if (!ok || *(volatile int*)abort_flag) {
-        // let the copies issued land before the CTA exits
-        for (int w = 0; w < kWarps; ++w) {
-          for (int64_t ch = issued_to > 0 ? issued_to - 1 : 0; ch < issued_to; ++ch) {
-            if (ch * kChunk + (int64_t)w * 2 * kKBlock >= K) continue;
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(&full[w], (uint32_t)ch & 1u) && global_ns() - t0 < 10000000ull) {
-            }
-          }
-        }
-      }
+  // this warp's two k-block buffers; buffer h holds k-block h of the warp's
+  // slice of one chunk at a time (stall: nothing is ever fetched, the
+  // bounded waits' test; 0 on every product call)
+  uint8_t* sl = smem + (size_t)warp * kSlice;
+  uint64_t* my_full = full + 2 * warp;
+  const int64_t kw = (int64_t)warp * 2 * kKBlock;  // the warp's first code in every chunk
+  auto fetch = [&](int h, int64_t k0) {  // lane 0 only
+    mbar_expect_tx(&my_full[h], kBuf);
+    tma_load_2d(sl + h * kBuf, &map_w, &my_full[h], (int)k0, (int)n0);
+    tma_load_2d(sl + h * kBuf + kWBox, &map_x, &my_full[h], (int)k0, 0);
+  };
+  uint32_t fetched[2] = {0u, 0u}, used[2] = {0u, 0u};  // per buffer (the same in every lane)
+  for (int h = 0; h < 2; ++h) {
+    if (!stall && kw + h * kKBlock < K) {
+      if (lane == 0) fetch(h, kw + h * kKBlock);
+      ++fetched[h];
     }
-  } else {
-    // ---------------- compute warps
-    const int cw = warp - 1;
-    const int g = lane >> 2, c = lane & 3;
-    // byte offsets of this lane's chunks 2c and 2c + 1 in a box row of
-    // the 8-row atom (128-byte swizzle: chunk XOR row-within-atom, here g)
-    const uint32_t off0 = (uint32_t)g * kKBlock + ((uint32_t)((2 * c) ^ g) << 4);
-    const uint32_t off1 = (uint32_t)g * kKBlock + ((uint32_t)((2 * c + 1) ^ g) << 4);
-    int32_t iacc[4][4];
+  }
+
+  const int g = lane >> 2, c = lane & 3;
+  // byte offsets of this lane's chunks 2c and 2c + 1 in a box row of the
+  // 8-row atom (128-byte swizzle: chunk XOR row-within-atom, here g)
+  const uint32_t off0 = (uint32_t)g * kKBlock + ((uint32_t)((2 * c) ^ g) << 4);
+  const uint32_t off1 = (uint32_t)g * kKBlock + ((uint32_t)((2 * c + 1) ^ g) << 4);
+  int32_t iacc[4][4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) iacc[t][r] = 0;
+  bool ok = true;
+  for (int64_t ch = 0; ok && ch < nchunks; ++ch) {
+    float facc[4][4];
 #pragma unroll
     for (int t = 0; t < 4; ++t)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) iacc[t][r] = 0;
-    for (int64_t ch = 0; ch < nchunks; ++ch) {
-      const int64_t k0 = ch * kChunk + (int64_t)cw * 2 * kKBlock;
-      if (k0 >= K) continue;  // nothing of this chunk for this warp (no copies, no barrier phase)
-      if (!__all_sync(0xFFFFFFFFu, wait(&full[cw], (uint32_t)ch & 1u))) break;
-      const uint8_t* sl = smem + (size_t)cw * kSlice;
-      float facc[4][4];
+      for (int r = 0; r < 4; ++r) facc[t][r] = 0.0f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
+    for (int h = 0; h < 2; ++h) {
+      const int64_t k0 = ch * kChunk + kw + h * kKBlock;
+      if (k0 >= K) break;  // this and every later k-block of the warp lie past K
+      if (!__all_sync(0xFFFFFFFFu, wait(&my_full[h], used[h] & 1u))) {
+        ok = false;
+        break;
+      }
+      ++used[h];
+      const uint8_t* wbox = sl + h * kBuf;
+      const uint8_t* xbox = wbox + kWBox;
+      // token fragments of the k-block: rows g and g + 8, chunks 2c and 2c + 1
+      uint32_t xa[2][2][8];  // [row g / g+8][chunk]
 #pragma unroll
-        for (int r = 0; r < 4; ++r) facc[t][r] = 0.0f;
-      const int nb = K - k0 > kKBlock ? 2 : 1;
+      for (int r = 0; r < 2; ++r) {
+        codes_to_f16(*reinterpret_cast<const uint4*>(xbox + r * 8 * kKBlock + off0), xa[r][0]);
+        codes_to_f16(*reinterpret_cast<const uint4*>(xbox + r * 8 * kKBlock + off1), xa[r][1]);
+      }
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        if (b >= nb) break;
-        const uint8_t* wbox = sl + b * kWBox;
-        const uint8_t* xbox = sl + 2 * kWBox + b * kXBox;
-        // token fragments of the k-block: rows g and g + 8, chunks 2c and 2c + 1
-        uint32_t xa[2][2][8];  // [row g / g+8][chunk]
+      for (int t = 0; t < 4; ++t) {  // channel tile: rows 8t + g
+        uint32_t wb[2][8];
+        codes_to_f16(*reinterpret_cast<const uint4*>(wbox + t * 8 * kKBlock + off0), wb[0]);
+        codes_to_f16(*reinterpret_cast<const uint4*>(wbox + t * 8 * kKBlock + off1), wb[1]);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          codes_to_f16(*reinterpret_cast<const uint4*>(xbox + r * 8 * kKBlock + off0), xa[r][0]);
-          codes_to_f16(*reinterpret_cast<const uint4*>(xbox + r * 8 * kKBlock + off1), xa[r][1]);
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {  // channel tile: rows 8t + g
-          uint32_t wb[2][8];
-          codes_to_f16(*reinterpret_cast<const uint4*>(wbox + t * 8 * kKBlock + off0), wb[0]);
-          codes_to_f16(*reinterpret_cast<const uint4*>(wbox + t * 8 * kKBlock + off1), wb[1]);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {  // k16 step j: codes 4(j % 4) .. +3 of chunk 2c + j / 4
-            const int h = j >> 2, p = 2 * (j & 3);
-            mma_f16(facc[t], xa[0][h][p], xa[1][h][p], xa[0][h][p + 1], xa[1][h][p + 1], wb[h][p],
-                    wb[h][p + 1]);
-          }
+        for (int j = 0; j < 8; ++j) {  // k16 step j: codes 4(j % 4) .. +3 of chunk 2c + j / 4
+          const int hh = j >> 2, p = 2 * (j & 3);
+          mma_f16(facc[t], xa[0][hh][p], xa[1][hh][p], xa[0][hh][p + 1], xa[1][hh][p + 1], wb[hh][p],
+                  wb[hh][p + 1]);
         }
       }
+      // every lane has read the buffer: refill it with the next chunk's k-block
       __syncwarp();
-      if (lane == 0) mbar_arrive_local(&empty[cw]);  // the slice is consumed
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) iacc[t][r] += __float2int_rn(facc[t][r]);
+      const int64_t kn = k0 + kChunk;
+      if (kn < K) {
+        if (lane == 0) fetch(h, kn);
+        ++fetched[h];
+      }
     }
-    // the warps' int32 sums meet in shared memory (every slice has been
-    // consumed, so no copy is still landing in the slices)
-    __syncwarp();
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-    int32_t* red = reinterpret_cast<int32_t*>(smem);  // [warp][token 16][channel 32]
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) iacc[t][r] += __float2int_rn(facc[t][r]);
+  }
+  if (!ok && lane == 0) {
+    // let this warp's copies in flight land before the shared memory is reused
+    for (int h = 0; h < 2; ++h) {
+      if (fetched[h] > used[h]) {
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(&my_full[h], used[h] & 1u) && global_ns() - t0 < 10000000ull) {
+        }
+      }
+    }
+  }
+  // the warps' int32 sums meet in shared memory (every buffer has been
+  // consumed, so no copy is still landing)
+  __syncthreads();
+  int32_t* red = reinterpret_cast<int32_t*>(smem);  // [warp][token 16][channel 32]
+  {
+    int32_t* r0 = red + (size_t)warp * 16 * kChan;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const int tk = g, chn = 8 * t + 2 * c;
-      int32_t* r0 = red + (size_t)cw * 16 * kChan;
-      r0[tk * kChan + chn] = iacc[t][0];
-      r0[tk * kChan + chn + 1] = iacc[t][1];
-      r0[(tk + 8) * kChan + chn] = iacc[t][2];
-      r0[(tk + 8) * kChan + chn + 1] = iacc[t][3];
+      const int chn = 8 * t + 2 * c;
+      r0[g * kChan + chn] = iacc[t][0];
+      r0[g * kChan + chn + 1] = iacc[t][1];
+      r0[(g + 8) * kChan + chn] = iacc[t][2];
+      r0[(g + 8) * kChan + chn + 1] = iacc[t][3];
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-    // consecutive threads take consecutive channels of one token: Y's rows
-    // are written in contiguous runs
-    for (int i = threadIdx.x - 32; i < 16 * kChan; i += kWarps * 32) {
-      const int tk = i / kChan, chn = i % kChan;
-      if (chn >= nch || tk >= M) continue;
-      int32_t a = 0;
+  }
+  __syncthreads();
+  // thread i: token i / 32, channel i % 32 (Y's rows written in contiguous runs)
+  if (has_out) {
+    int32_t a = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) a += red[(size_t)w * 16 * kChan + i];
-      const int64_t n = n0 + chn;
-      const float v = __fmul_rn(__fmul_rn(__int2float_rn(a), x_scale[tk]), w_scale[n]);
-      y[(int64_t)tk * N + n] = __float2bfloat16_rn(v);
-      if (acc_out) acc_out[(int64_t)tk * N + n] = a;
-    }
+    for (int w = 0; w < kWarps; ++w) a += red[(size_t)w * 16 * kChan + threadIdx.x];
+    const int64_t n = n0 + out_ch;
+    const float v = __fmul_rn(__fmul_rn(__int2float_rn(a), xs), wsc);
+    y[(int64_t)out_tk * N + n] = __float2bfloat16_rn(v);
+    if (acc_out) acc_out[(int64_t)out_tk * N + n] = a;
   }
 }
 
