@@ -14,8 +14,10 @@ import torch
 
 from . import sq
 
-# Token count from which the bf16-coded tensor-core GEMM is used; below it
-# the step streams int8 weight codes through the integer mma.sync path.
+# Token count from which the codes are stored as bf16 values for the
+# tensor-core GEMM that TMA-loads them as they are (faster than widening
+# 1-byte codes on chip); below it the step streams 1-byte weight codes
+# through the weight-streaming kernels.
 TENSOR_PATH_MIN_TOKENS = 64
 # Above this token count the library runs 1-byte codes on the tensor cores
 # (the int8-operand tcgen05 kernel), at or below it on mma.sync.
