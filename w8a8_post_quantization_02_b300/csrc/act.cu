@@ -299,16 +299,22 @@ __global__ void __launch_bounds__(NT) k_quant_act(const uint8_t* __restrict__ x,
           bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
         }
       }
-      // block: align the warps' sums to the row's largest exponent (every
-      // thread forms the same total in the same order)
-      int eb = 1;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) eb = max(eb, (int)red_e[(it & 1) * NW + w]);
+      // block: lane w of every warp aligns warp w's sum to the row's largest
+      // exponent, and a butterfly over the first NW lanes adds them (integer
+      // sums: the order does not matter)
+      static_assert((NW & (NW - 1)) == 0 && NW <= 32, "power-of-two warp count");
+      const int ew_l = lane < NW ? (int)red_e[(it & 1) * NW + lane] : 1;
+      const int eb = (int)__reduce_max_sync(0xFFFFFFFFu, (uint32_t)ew_l);
       const bool row_finite = eb < 255;
       U128 tot = {0ull, 0ull};
+      if (lane < NW) tot = shr128(red_s[(it & 1) * NW + lane], 2 * (eb - ew_l));
 #pragma unroll
-      for (int w = 0; w < NW; ++w)
-        tot = add128(tot, shr128(red_s[(it & 1) * NW + w], 2 * (eb - (int)red_e[(it & 1) * NW + w])));
+      for (int o = NW / 2; o > 0; o >>= 1) {
+        U128 other;
+        other.hi = __shfl_xor_sync(0xFFFFFFFFu, tot.hi, o);
+        other.lo = __shfl_xor_sync(0xFFFFFFFFu, tot.lo, o);
+        tot = add128(tot, other);
+      }
       // r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))), S the exact sum rounded
       // once to binary32, every step one IEEE binary32 operation
       float rn32 = 0.0f;
