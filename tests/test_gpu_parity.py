@@ -741,7 +741,9 @@ def test_rmsnorm_nonfinite_flag(sq):
 
 # ------------------------------------------------------------------ Smooth Rotation
 ROT_ACT_SHAPES = [(64, 512, "f32"), (37, 256, "bf16"), (5, 512, "bf16"), (300, 4096, "bf16"), (9, 8192, "f32"),
-                  (129, 16384, "bf16"), (40, 32768, "bf16"), (77, 11008, "bf16")]
+                  (129, 16384, "bf16"), (40, 32768, "bf16"), (77, 11008, "bf16"),
+                  # rows of 2^10 .. 2^14 take the three-phase transform: every length, both input types
+                  (33, 1024, "bf16"), (17, 2048, "f32"), (50, 8192, "bf16"), (3, 16384, "f32"), (21, 1024, "f32")]
 
 
 @pytest.mark.parametrize("qmax", [7, 127])
@@ -765,7 +767,7 @@ def test_rotate_quant_act_bit_exact(sq, tokens, cin, dtype, qmax):
 
 
 ROT_W_SHAPES = [(256, 40, "bf16"), (4096, 264, "bf16"), (8192, 72, "bf16"), (512, 33, "f32"),
-                (11008, 24, "bf16")]
+                (11008, 24, "bf16"), (1024, 40, "bf16"), (2048, 24, "f32"), (16384, 8, "bf16")]
 
 
 @pytest.mark.parametrize("qmax", [7, 127])
