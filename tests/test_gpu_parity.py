@@ -390,6 +390,9 @@ FOLD_SHAPES = [
     (768, 40, "bf16"), (1536, 96, "bf16"), (1552, 40, "bf16"), (4096, 264, "bf16"), (6144, 136, "bf16"),
     (6160, 72, "bf16"), (12288, 32, "bf16"), (12304, 24, "bf16"), (2048, 20, "f32"),
     (48, 1000, "f32"),
+    # whole 64-channel strips of bf16 W: clusters of 1-8 CTAs with ragged last CTAs, and a box
+    # running past the last row
+    (4096, 128, "bf16"), (1040, 64, "bf16"), (48, 64, "bf16"), (2064, 192, "bf16"), (8192, 320, "bf16"),
 ]
 
 
