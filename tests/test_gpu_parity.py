@@ -317,6 +317,9 @@ def test_gemm_saturated_widest_k(sq, codes):
     (8, 4096, 4096), (16, 100, 2064), (3, 33, 16), (16, 4096, 11008), (9, 72, 560),
     # more than 8192 codes of K per CTA: several exact fp32 chunks per CTA
     (16, 24, 66048), (3, 200, 70000),
+    # more tiles than CTA pairs (or CTAs), a partial last wave: a K tail, a
+    # ragged M, several chunks per tile, one-CTA tiles
+    (2048, 5120, 1040), (520, 8192, 2048), (300, 20000, 3088), (64, 40000, 256),
     # int8 codes: weight rows staged in shared memory up to K = 12288 (a
     # ragged last block of rows, M in each of the 16/32/64-token tilings),
     # the register-fed kernel beyond it
