@@ -31,6 +31,8 @@
 // outstanding copies and MMAs, frees TMEM and returns.
 #include "sq_tc.cuh"
 
+#include <cstring>
+
 namespace sq {
 namespace tc {
 
@@ -58,6 +60,14 @@ struct Cfg {
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(B_ROWS % 8 == 0, "whole 8-row swizzle atoms");
   static_assert(COLS % 8 == 0, "epilogue works in 8-column groups");
+  // Y leaves through shared memory: each epilogue warp stages 32 rows x
+  // SLICE columns and stores them with one TMA copy.  40-column rows (80
+  // bytes) are written without bank conflicts as they are; 32-column rows
+  // (64 bytes) use the 64-byte swizzle.
+  static constexpr int SLICE = COLS % 40 == 0 ? 40 : 32;
+  static constexpr int SLICE_BYTES = 32 * SLICE * 2;
+  static constexpr bool SW64 = SLICE == 32;
+  static_assert(COLS % SLICE == 0 && SLICE % 8 == 0, "whole 16-byte groups per slice");
 };
 
 template <int CG, int BN>
@@ -65,6 +75,10 @@ struct Smem {
   using C = Cfg<CG, BN>;
   uint8_t a[C::STAGES][A_BYTES];
   uint8_t b[C::STAGES][C::B_BYTES];
+  // each epilogue warp's w_scale slice for the current tile, loaded when the
+  // tile starts so the output pass reads it from shared memory
+  alignas(16) float ws[EPI_WARPS][C::COLS];
+  alignas(1024) uint8_t ystage[EPI_WARPS][C::SLICE_BYTES];
   uint64_t full[C::STAGES];
   uint64_t empty[C::STAGES];
   uint64_t acc_full[2];
@@ -78,14 +92,26 @@ struct Problem {
   int64_t M, N, K;
   int tiles_m, tiles_n, n_kb, n_chunks;
   int vec_ok;  // N % 8 == 0 and y / acc_out 16-byte aligned: 16-byte stores
+  int tma_y;   // N % 8 == 0 and y 16-byte aligned: Y leaves by TMA stores
   int stall;   // the producer issues no copies (the bounded waits' test): 0 on every product call
   uint64_t wait_ns;  // bound on every pipeline wait
 };
+
+// Eight floats rounded to bf16, packed in column order.
+SQ_DEVINL uint4 pack_bf16x8(const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i])) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1])) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // ------------------------------------------------------------------ kernel
 template <int CG, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_bf16c(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                 const __grid_constant__ CUtensorMap map_y,
                  const float* __restrict__ x_scale, const float* __restrict__ w_scale,
                  __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out, int32_t* flags,
                  Problem P) {
@@ -233,6 +259,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = unit; ok && tile < num_tiles; tile += n_units) {
       const int64_t m0 = (int64_t)(tile % P.tiles_m) * C::MMA_M + (int64_t)rank * BM;
       const int64_t n0 = (int64_t)(tile / P.tiles_m) * BN;
+      const int64_t m = m0 + q * 32 + lane;
+      const int64_t nb = n0 + half * C::COLS;
+      // the scales' L2 round trips overlap the wait for the first chunk
+      float* wsw = sm.ws[warp - 2];
+      __syncwarp();  // the previous tile's reads of wsw are done
+      for (int i = lane; i < C::COLS; i += 32) wsw[i] = (nb + i < P.N) ? __ldg(w_scale + nb + i) : 0.0f;
+      const float xs = (m < P.M) ? __ldg(x_scale + m) : 0.0f;
+      __syncwarp();
       int32_t acc[C::COLS];
 #pragma unroll
       for (int i = 0; i < C::COLS; ++i) acc[i] = 0;
@@ -275,32 +309,65 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++chunk_ctr;
       }
       if (!ok) break;
-      const int64_t m = m0 + q * 32 + lane;
-      if (m < P.M) {
-        const float xs = x_scale[m];
-        const int64_t nb = n0 + half * C::COLS;
+      if (P.tma_y) {
+        // stage 32 rows x SLICE columns, then one TMA store per slice
+        uint8_t* stg = sm.ystage[warp - 2];
+        const int64_t row0 = m0 + q * 32;
+#pragma unroll
+        for (int sl = 0; sl < C::COLS / C::SLICE; ++sl) {
+          if (lane == 0) async::bulk_wait_read_all();  // the previous slice has left shared memory
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < C::SLICE / 8; ++g) {
+            const int gg = sl * (C::SLICE / 8) + g;
+            const float4 w0 = *reinterpret_cast<const float4*>(wsw + gg * 8);
+            const float4 w1 = *reinterpret_cast<const float4*>(wsw + gg * 8 + 4);
+            const float ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__fmul_rn(__int2float_rn(acc[gg * 8 + e]), xs), ws[e]);
+            const int chunk = C::SW64 ? (g ^ ((lane >> 1) & 3)) : g;
+            *reinterpret_cast<uint4*>(stg + lane * (C::SLICE * 2) + chunk * 16) = pack_bf16x8(v);
+          }
+          async::fence_proxy_async_smem();
+          __syncwarp();
+          const int64_t ns = nb + sl * C::SLICE;
+          if (lane == 0 && row0 < P.M && ns < P.N) {
+            async::tma_store_2d(&map_y, stg, (int)ns, (int)row0);
+            async::bulk_commit();
+          }
+        }
+        if (acc_out != nullptr && m < P.M) {
+          // the exact accumulators, for callers that ask for them
+#pragma unroll
+          for (int g = 0; g < C::COLS / 8; ++g) {
+            const int64_t n = nb + g * 8;
+            if (n >= P.N) break;
+            int32_t* arow = acc_out + m * P.N + n;
+            if (n + 8 <= P.N && P.vec_ok) {
+              st16(arow, make_uint4(acc[g * 8 + 0], acc[g * 8 + 1], acc[g * 8 + 2], acc[g * 8 + 3]));
+              st16(arow + 4, make_uint4(acc[g * 8 + 4], acc[g * 8 + 5], acc[g * 8 + 6], acc[g * 8 + 7]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (n + e < P.N) arow[e] = acc[g * 8 + e];
+            }
+          }
+        }
+      } else if (m < P.M) {
 #pragma unroll
         for (int g = 0; g < C::COLS / 8; ++g) {
           const int64_t n = nb + g * 8;
           if (n >= P.N) break;
+          const float4 w0 = *reinterpret_cast<const float4*>(wsw + g * 8);
+          const float4 w1 = *reinterpret_cast<const float4*>(wsw + g * 8 + 4);
+          const float ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
           float v[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float ws = (n + e < P.N) ? __ldg(w_scale + n + e) : 0.0f;
-            v[e] = __fmul_rn(__fmul_rn(__int2float_rn(acc[g * 8 + e]), xs), ws);
-          }
+          for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__fmul_rn(__int2float_rn(acc[g * 8 + e]), xs), ws[e]);
           __nv_bfloat16* yrow = y + m * P.N + n;
           if (n + 8 <= P.N && P.vec_ok) {
-            uint4 o;
-            o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[0])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[1])) << 16);
-            o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[3])) << 16);
-            o.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[4])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[5])) << 16);
-            o.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[6])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[7])) << 16);
-            st16(yrow, o);
+            st16(yrow, pack_bf16x8(v));
             if (acc_out) {
               int32_t* arow = acc_out + m * P.N + n;
               st16(arow, make_uint4(acc[g * 8 + 0], acc[g * 8 + 1], acc[g * 8 + 2], acc[g * 8 + 3]));
@@ -318,6 +385,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+    // the staged Y slices are written before the CTA's shared memory goes
+    if (lane == 0) async::bulk_wait_all();
   }
 
   tc_fence_before();
@@ -351,6 +420,22 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint3
   return r == CUDA_SUCCESS;
 }
 
+// Y [m x n] bf16 (n contiguous) for the epilogue's TMA stores: boxes of
+// `slice` columns x 32 rows, 64-byte swizzle when a box row is 64 bytes.
+bool make_map_y(CUtensorMap* map, void* y, int64_t m, int64_t n, uint32_t slice) {
+  auto fn = async::tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)m};
+  cuuint64_t strides[1] = {(cuuint64_t)n * 2};
+  cuuint32_t box[2] = {slice, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  slice * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int CG, int BN>
 sq_status launch(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
                  int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
@@ -374,6 +459,9 @@ sq_status launch(const void* xq, const float* x_scale, const void* wq, const flo
   P.n_kb = (int)((k + BK - 1) / BK);
   P.n_chunks = (P.n_kb + CHUNK_KB - 1) / CHUNK_KB;
   P.vec_ok = (n % 8 == 0) && aligned16(y) && (acc_out == nullptr || aligned16(acc_out));
+  CUtensorMap my;
+  std::memset(&my, 0, sizeof(my));
+  P.tma_y = (n % 8 == 0) && aligned16(y) && make_map_y(&my, y, m, n, C::SLICE) ? 1 : 0;
   P.stall = stall;
   P.wait_ns = wait_ns;
   const int tiles = P.tiles_m * P.tiles_n;
@@ -390,7 +478,7 @@ sq_status launch(const void* xq, const float* x_scale, const void* wq, const flo
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, ma, mb, x_scale, w_scale, static_cast<__nv_bfloat16*>(y),
+  if (cudaLaunchKernelEx(&cfg, kern, ma, mb, my, x_scale, w_scale, static_cast<__nv_bfloat16*>(y),
                          acc_out, flags, P) != cudaSuccess)
     return SQ_ERR_CUDA;
   return launch_status();
