@@ -266,8 +266,8 @@ def to_device(case, torch):
 # on the same workload (dram__bytes_read.sum + dram__bytes_write.sum), or
 # absent when the kernel changed after the capture.
 NCU_TRAFFIC_BYTES = {
-    # 109.33 MB read + 25.78 MB written (the rest of Y still dirty in L2)
-    ("k_gemm_bf16c", "prefill_upgate_2048x4096x11008"): 135.11e6,
+    # 107.96 MB read + 26.16 MB written (the rest of Y still dirty in L2)
+    ("k_gemm_bf16c", "prefill_upgate_2048x4096x11008"): 134.12e6,
     # 53.87 MB read (the int8 codes of X and W, once) + 9.99 MB written
     ("k_gemm_i8c", "prefill_upgate_2048x4096x11008"): 63.86e6,
     # 16.88 MB read (the int8 weight codes and X codes), nothing written back yet
