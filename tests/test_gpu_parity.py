@@ -337,6 +337,36 @@ def test_gemm_shapes_random_codes(sq, codes, m, n, k):
 
 
 
+
+@pytest.mark.parametrize("codes", gemm_code_formats())
+@pytest.mark.parametrize("m,n,k", [(130, 264, 1040), (100, 520, 1040), (300, 2000, 2064)])
+@pytest.mark.parametrize("offset", [2, 8])
+def test_gemm_y_alignment_no_acc(sq, codes, m, n, k, offset):
+    """Y written into a buffer 4 bytes (offset 2) or 16 bytes (offset 8) past
+    an allocation, with no accumulators requested: the epilogue's TMA-store
+    path needs N % 8 == 0 and a 16-byte aligned Y, and takes direct stores
+    otherwise.  The bytes around Y stay untouched."""
+    u = synth.uniform(m + n + k + offset, 9, (m + n) * k)
+    codes_all = np.clip(np.floor(u * 255.0) - 127.0, -127, 127).astype(np.int8)
+    xq, wq = codes_all[: m * k].reshape(m, k), codes_all[m * k:].reshape(n, k)
+    xs = (0.001 + synth.uniform(1, 10, m)).astype(F32)
+    ws = (0.0001 + synth.uniform(1, 11, n) * 0.01).astype(F32)
+    if codes == "bf16":
+        xt = torch.from_numpy(xq.astype(F32)).to(torch.bfloat16).cuda()
+        wt = torch.from_numpy(wq.astype(F32)).to(torch.bfloat16).cuda()
+    else:
+        xt, wt = torch.from_numpy(xq).cuda(), torch.from_numpy(wq).cuda()
+    sentinel = torch.tensor(-12345.0, dtype=torch.bfloat16)
+    buf = torch.full((m * n + offset + 8,), float(sentinel), dtype=torch.bfloat16, device="cuda")
+    y = buf[offset: offset + m * n].view(m, n)
+    assert y.data_ptr() % 16 == (0 if offset == 8 else 4)
+    sq.w8a8_gemm(xt, torch.from_numpy(xs).cuda(), wt, torch.from_numpy(ws).cuda(),
+                 flags=flags_tensor(), out=y)
+    _, ref_y = O.w8a8_gemm(xq, xs, wq, ws)
+    assert O.bf16_ulp_distance(y_bits(y), ref_y).max() <= 1
+    rest = torch.cat([buf[:offset], buf[offset + m * n:]]).cpu()
+    assert torch.all(rest == sentinel)
+
 def carrier_adversarial_codes(m, n, k, seed):
     """Codes built against the fp32 carrier of the tensor-core GEMM.
 
