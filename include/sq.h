@@ -311,7 +311,11 @@ sq_status sq_rotate_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin
  *   wq     device [n x k] codes, format fmt (K contiguous)
  *   y      device bf16 [m x n] row-major
  *   acc_out  device int32 [m x n] or NULL: the exact accumulators
- *   workspace  device, >= sq_workspace_bytes(SQ_OP_GEMM, m, n, k, fmt)
+ *   workspace  device, 16-byte aligned; sq_workspace_bytes(SQ_OP_GEMM, m, n,
+ *              k, fmt) bytes (0 for SQ_CODES_BF16 and for m <= 64;
+ *              (m + n) * k * 2 rounded up to 256 for SQ_CODES_I8 with
+ *              m > 64).  A smaller or NULL workspace is not an error: the
+ *              call then takes the path that needs none (below).
  * k must be a multiple of 16 and at most SQ_GEMM_MAX_K (beyond it a sum of
  * k products of 127 * 127 could leave int32: SQ_ERR_UNSUPPORTED).
  * SQ_CODES_BF16 runs on the tcgen05 tensor
@@ -319,8 +323,11 @@ sq_status sq_rotate_fold_quantize_weight(const void* w, sq_dtype dt, int64_t cin
  * products so every partial sum stays an exact integer).  SQ_CODES_I8 reads
  * one byte per code: m <= 16 runs the weight-streaming decode kernel
  * (codes widened to fp16 on chip, mma.sync), 16 < m <= 64 the integer
- * mma.sync kernel, m > 64 the tcgen05 tensor cores with the codes widened
- * to fp16 in shared memory; every path accumulates exactly.
+ * mma.sync kernel, m > 64 the tcgen05 tensor cores: with the workspace, one
+ * pass widens both operands' codes to exact fp16 values in it and the
+ * 16-bit-carrier kernel multiplies them (two kernels); without it, one
+ * kernel widens the codes in shared memory as it goes (slower: the
+ * shared-memory banks carry the widening).  Every path accumulates exactly.
  * A pipeline wait that runs out sets SQ_FLAG_TIMEOUT.
  */
 #define SQ_GEMM_MAX_K 133136 /* largest multiple of 16 with k * 127^2 < 2^31 */
@@ -422,9 +429,11 @@ size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fm
 
 /*
  * Number of kernels one call of `op` enqueues for these sizes, assuming
- * every pointer is 16-byte aligned: `ld` is the leading dimension (in
- * elements, type dt) of the call's input matrix, `axis` and `accumulate`
- * matter for SQ_OP_CALIBRATE only.  Sizes follow each entry point's own
+ * every pointer is 16-byte aligned and every workspace has the size
+ * sq_workspace_bytes asks for: `ld` is the leading dimension (in elements,
+ * type dt) of the call's input matrix; `axis` and `accumulate` are
+ * SQ_OP_CALIBRATE's, except that for SQ_OP_GEMM `axis` carries the code
+ * format (sq_codes).  Sizes follow each entry point's own
  * names: calibrate (m = rows, n = cols), smooth (k = cin), fold
  * (k = cin, n = cout), quant_act (m = tokens, k = cin), GEMM (m, n, k).
  * For budgeting launches (e.g. in a CUDA graph) and reading a profiler's

@@ -367,6 +367,25 @@ def test_gemm_y_alignment_no_acc(sq, codes, m, n, k, offset):
     rest = torch.cat([buf[:offset], buf[offset + m * n:]]).cpu()
     assert torch.all(rest == sentinel)
 
+
+@pytest.mark.parametrize("m,n,k", [(65, 300, 2064), (130, 257, 1040), (520, 3080, 272), (300, 1000, 3088)])
+def test_gemm_i8_without_workspace(sq, m, n, k):
+    """1-byte codes above 64 tokens given a workspace too small for the
+    widened operands: the kernel that widens the codes in shared memory as
+    it goes (the default, with the workspace, widens them in one pass
+    first).  Both are exact."""
+    u = synth.uniform(m + n + k, 12, (m + n) * k)
+    codes_all = np.clip(np.floor(u * 255.0) - 127.0, -127, 127).astype(np.int8)
+    xq, wq = codes_all[: m * k].reshape(m, k), codes_all[m * k:].reshape(n, k)
+    xs = (0.001 + synth.uniform(1, 13, m)).astype(F32)
+    ws = (0.0001 + synth.uniform(1, 14, n) * 0.01).astype(F32)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    y, acc = sq.w8a8_gemm(torch.from_numpy(xq).cuda(), torch.from_numpy(xs).cuda(), torch.from_numpy(wq).cuda(),
+                          torch.from_numpy(ws).cuda(), want_acc=True, flags=flags_tensor(), workspace=small)
+    ref_acc, ref_y = O.w8a8_gemm(xq, xs, wq, ws)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref_acc)
+    assert O.bf16_ulp_distance(y_bits(y), ref_y).max() <= 1
+
 def carrier_adversarial_codes(m, n, k, seed):
     """Codes built against the fp32 carrier of the tensor-core GEMM.
 

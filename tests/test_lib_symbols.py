@@ -50,6 +50,10 @@ def test_workspace_sizes(lib):
     from w8a8_post_quantization_02_b300 import sq
     assert h.sq_workspace_bytes(sq.SQ_OP_FOLD_QUANTIZE, 0, 11008, 4096, 0) >= 11008 * 4
     assert h.sq_workspace_bytes(sq.SQ_OP_QUANT_ACT, 2048, 0, 4096, 0) == 0
+    # GEMM: the widened fp16 operands of 1-byte codes above 64 tokens
+    assert h.sq_workspace_bytes(sq.SQ_OP_GEMM, 2048, 11008, 4096, sq.SQ_CODES_I8) == (2048 + 11008) * 4096 * 2
+    assert h.sq_workspace_bytes(sq.SQ_OP_GEMM, 2048, 11008, 4096, sq.SQ_CODES_BF16) == 0
+    assert h.sq_workspace_bytes(sq.SQ_OP_GEMM, 64, 11008, 4096, sq.SQ_CODES_I8) == 0
 
 
 def test_argument_validation_needs_no_device(lib):
@@ -123,8 +127,13 @@ def test_kernel_counts_need_no_device(lib):
     assert h.sq_kernel_count(sq.SQ_OP_FOLD_QUANTIZE, sq.SQ_BF16, 0, 4096, 11008, 4096, 0, 0) == 1
     assert h.sq_kernel_count(sq.SQ_OP_FOLD_QUANTIZE, sq.SQ_BF16, 0, 300, 80, 300, 0, 0) == 3
     assert h.sq_kernel_count(sq.SQ_OP_FOLD_QUANTIZE, sq.SQ_BF16, 0, 64, 12304, 64, 0, 0) == 3
-    for op in (sq.SQ_OP_SMOOTH, sq.SQ_OP_QUANT_ACT, sq.SQ_OP_GEMM):
+    for op in (sq.SQ_OP_SMOOTH, sq.SQ_OP_QUANT_ACT):
         assert h.sq_kernel_count(op, sq.SQ_BF16, 2048, 11008, 4096, 4096, 0, 0) == 1
+    # GEMM (axis: the code format): one kernel, except 1-byte codes above 64
+    # tokens, which are widened in the workspace first
+    assert h.sq_kernel_count(sq.SQ_OP_GEMM, sq.SQ_BF16, 2048, 11008, 4096, 0, sq.SQ_CODES_BF16, 0) == 1
+    assert h.sq_kernel_count(sq.SQ_OP_GEMM, sq.SQ_BF16, 2048, 11008, 4096, 0, sq.SQ_CODES_I8, 0) == 2
+    assert h.sq_kernel_count(sq.SQ_OP_GEMM, sq.SQ_BF16, 64, 11008, 4096, 0, sq.SQ_CODES_I8, 0) == 1
     assert h.sq_kernel_count(99, sq.SQ_BF16, 1, 1, 16, 16, 0, 0) == -1
 
 

@@ -35,7 +35,10 @@ int calibrate_kernel_count(sq_dtype, int64_t, int64_t, int64_t, int, int);
 sq_status gemm_i8_mma(const int8_t*, const float*, const int8_t*, const float*, int64_t, int64_t,
                       int64_t, void*, int32_t*, cudaStream_t);
 sq_status gemm_bf16c_tc(const void*, const float*, const void*, const float*, int64_t, int64_t,
-                        int64_t, void*, int32_t*, int32_t*, uint64_t, int, cudaStream_t);
+                        int64_t, void*, int32_t*, int32_t*, uint64_t, int, cudaStream_t, bool);
+sq_status gemm_i8_widened_tc(const void*, const float*, const void*, const float*, int64_t, int64_t,
+                             int64_t, void*, int32_t*, int32_t*, void*, uint64_t, int, cudaStream_t);
+size_t gemm_widen_bytes(int64_t, int64_t, int64_t);
 sq_status gemm_i8c_tc(const void*, const float*, const void*, const float*, int64_t, int64_t,
                       int64_t, void*, int32_t*, int32_t*, uint64_t, int, cudaStream_t);
 sq_status quant_act_stalled(const void*, sq_dtype, int64_t, int64_t, int64_t, const float*, void*,
@@ -97,12 +100,12 @@ sq_status sq_check_device(int device) {
 }
 
 size_t sq_workspace_bytes(sq_op op, int64_t m, int64_t n, int64_t k, sq_codes fmt) {
-  (void)m;
-  (void)k;
-  (void)fmt;
   switch (op) {
     case SQ_OP_FOLD_QUANTIZE: return n > 0 ? round256((size_t)n * 4) : 0;
     case SQ_OP_ROTATE_WEIGHT: return (n > 0 && k > 0) ? round256((size_t)n * (size_t)k * 4) : 0;
+    case SQ_OP_GEMM:  // 1-byte codes on the tensor cores: both operands widened to fp16
+      return (fmt == SQ_CODES_I8 && m > kI8TensorCoreMinM && n > 0 && k > 0) ? round256(gemm_widen_bytes(m, n, k))
+                                                                              : 0;
     default: return 0;
   }
 }
@@ -120,7 +123,8 @@ int sq_kernel_count(sq_op op, sq_dtype dt, int64_t m, int64_t n, int64_t k, int6
     case SQ_OP_RMSNORM_QUANT_ACT: return 1;
     case SQ_OP_ROTATE_ACT: return 1;
     case SQ_OP_ROTATE_WEIGHT: return 2;
-    case SQ_OP_GEMM: return 1;
+    case SQ_OP_GEMM:  // axis: the code format (sq_codes)
+      return (axis == SQ_CODES_I8 && m > kI8TensorCoreMinM) ? 2 : 1;
   }
   return -1;
 }
@@ -294,7 +298,8 @@ namespace {
 sq_status w8a8_gemm_dispatch(const void* xq, const float* x_scale, const void* wq,
                              const float* w_scale, sq_codes fmt, int64_t m, int64_t n, int64_t k,
                              void* y, int32_t* acc_out, int32_t* dev_flags, uint64_t wait_ns,
-                             int stall, cudaStream_t stream) {
+                             int stall, cudaStream_t stream, void* workspace = nullptr,
+                             size_t ws_bytes = 0) {
   if (!xq || !x_scale || !wq || !w_scale || !y || !valid_codes(fmt) || m < 1 || n < 1 || k < 16 ||
       k % 16 != 0)
     return SQ_ERR_INVALID_ARG;
@@ -310,9 +315,17 @@ sq_status w8a8_gemm_dispatch(const void* xq, const float* x_scale, const void* w
     return gemm_i8_mma(static_cast<const int8_t*>(xq), x_scale, static_cast<const int8_t*>(wq),
                        w_scale, m, n, k, y, acc_out, stream);
   }
-  if (fmt == SQ_CODES_I8)
+  if (fmt == SQ_CODES_I8) {
+    // with room for the widened operands: one pass widens both to fp16 and
+    // the 16-bit-carrier kernel runs; otherwise the kernel that widens in
+    // shared memory as it goes
+    if (workspace && aligned16(workspace) && ws_bytes >= gemm_widen_bytes(m, n, k))
+      return gemm_i8_widened_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, workspace,
+                                wait_ns, stall, stream);
     return gemm_i8c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, wait_ns, stall, stream);
-  return gemm_bf16c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, wait_ns, stall, stream);
+  }
+  return gemm_bf16c_tc(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, dev_flags, wait_ns, stall, stream,
+                       false);
 }
 }  // namespace
 
@@ -320,10 +333,8 @@ sq_status sq_w8a8_gemm(const void* xq, const float* x_scale, const void* wq, con
                        sq_codes fmt, int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out,
                        int32_t* dev_flags, void* workspace, size_t ws_bytes,
                        cudaStream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
   return w8a8_gemm_dispatch(xq, x_scale, wq, w_scale, fmt, m, n, k, y, acc_out, dev_flags, kGemmWaitNs,
-                            0, stream);
+                            0, stream, workspace, ws_bytes);
 }
 
 sq_status sq_test_w8a8_gemm_stalled(const void* xq, const float* x_scale, const void* wq,

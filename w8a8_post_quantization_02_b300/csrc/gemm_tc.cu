@@ -26,7 +26,8 @@
 //     shared memory and write each CTA's own 128 accumulator lanes.  Per
 //     SM this moves 2/3 of the operand bytes of the one-CTA tile.
 // BN (the output-channel tile, 256 or 240) is chosen per problem to fill
-// the last wave of tiles.  Every mbarrier wait is bounded in time; a wait that runs out
+// the last wave of tiles.  With F16 the operands are exact fp16 values
+// instead (the same integers; 1-byte codes widened by k_widen_codes below).  Every mbarrier wait is bounded in time; a wait that runs out
 // sets SQ_FLAG_TIMEOUT, stops the CTA's loops, waits (bounded) for its own
 // outstanding copies and MMAs, frees TMEM and returns.
 #include "sq_tc.cuh"
@@ -54,6 +55,8 @@ struct Cfg {
   static constexpr int MMA_M = BM * CG;
   // instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
   // (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24
+  // fp16 operands: A and B formats 0 in bits 7-9 and 10-12
+  static constexpr uint32_t IDESC_F16 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
   static constexpr int COLS = BN / 2;  // accumulator columns per epilogue warp
@@ -108,7 +111,7 @@ SQ_DEVINL uint4 pack_bf16x8(const float (&v)[8]) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <int CG, int BN>
+template <int CG, int BN, bool F16>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_bf16c(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const __grid_constant__ CUtensorMap map_y,
@@ -227,7 +230,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t a_addr = su32(sm.a[stage]), b_addr = su32(sm.b[stage]);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_f16<CG>(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), C::IDESC,
+              mma_f16<CG>(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                          F16 ? C::IDESC_F16 : C::IDESC,
                            (kb > kb0 || kk > 0) ? 1u : 0u);
             mma_commit<CG>(&sm.empty[stage]);
             if (++stage == C::STAGES) {
@@ -407,14 +411,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ------------------------------------------------------------------ host side
 // 2-D bf16 tensor [rows x k] (k contiguous), box of 64 x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint32_t box_rows) {
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint32_t box_rows, bool f16) {
   auto fn = async::tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)k * 2};
   cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -436,14 +441,14 @@ bool make_map_y(CUtensorMap* map, void* y, int64_t m, int64_t n, uint32_t slice)
   return r == CUDA_SUCCESS;
 }
 
-template <int CG, int BN>
+template <int CG, int BN, bool F16>
 sq_status launch(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
                  int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
                  uint64_t wait_ns, int stall, cudaStream_t st) {
   using C = Cfg<CG, BN>;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, xq, m, k, BM) || !make_map(&mb, wq, n, k, C::B_ROWS)) return SQ_ERR_CUDA;
-  auto kern = k_gemm_bf16c<CG, BN>;
+  if (!make_map(&ma, xq, m, k, BM, F16) || !make_map(&mb, wq, n, k, C::B_ROWS, F16)) return SQ_ERR_CUDA;
+  auto kern = k_gemm_bf16c<CG, BN, F16>;
   const size_t smem = sizeof(Smem<CG, BN>) + 1024;
   static std::atomic<uint64_t> attr_done{0};
   if (!once_per_device(attr_done, [&] {
@@ -507,14 +512,133 @@ int gemm_bf16c_cta_group(int64_t m) { return m > tc::BM ? 2 : 1; }
 
 sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
                         int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
-                        uint64_t wait_ns, int stall, cudaStream_t st) {
+                        uint64_t wait_ns, int stall, cudaStream_t st, bool f16) {
   using namespace tc;
   if (m > (int64_t)1 << 31 || n > (int64_t)1 << 31 || k > (int64_t)1 << 31) return SQ_ERR_UNSUPPORTED;
-  if (gemm_bf16c_cta_group(m) == 1)
-    return launch<1, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
-  if (choose_bn(m, n, sm_count() / 2, 2 * BM) == 240)
-    return launch<2, 240>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
-  return launch<2, 256>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, stall, st);
+  const int cg = gemm_bf16c_cta_group(m);
+  const int bn = cg == 1 ? 256 : choose_bn(m, n, sm_count() / 2, 2 * BM);
+#define SQ_TC_LAUNCH(CG_, BN_)                                                                     \
+  return f16 ? launch<CG_, BN_, true>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, \
+                                      stall, st)                                                    \
+             : launch<CG_, BN_, false>(xq, x_scale, wq, w_scale, m, n, k, y, acc_out, flags, wait_ns, \
+                                       stall, st)
+  if (cg == 1) SQ_TC_LAUNCH(1, 256);
+  if (bn == 240) SQ_TC_LAUNCH(2, 240);
+  SQ_TC_LAUNCH(2, 256);
+#undef SQ_TC_LAUNCH
+}
+
+// 1-byte codes widened to exact fp16 values (flip the sign bit, place the
+// byte in the significand of 1024 + u, subtract 1152: every step exact).
+// The codes of a (na bytes) and then b (nb bytes) are cut into chunks of
+// kWidenChunk bytes (a's last chunk may be short, and b's); chunk c goes to
+// block c mod gridDim.  One thread per block bulk-copies the block's chunks
+// into a ring of kWidenStages buffers; every thread widens 8-code units of
+// the current buffer and writes them to dst (16 bytes per unit, in order).
+// Every wait on the ring is bounded; one that runs out sets
+// SQ_FLAG_TIMEOUT and the block stops after its copies have landed.
+constexpr int kWidenThreads = 256;
+constexpr int kWidenChunk = 8192;
+constexpr int kWidenStages = 4;
+__global__ void __launch_bounds__(kWidenThreads) k_widen_codes(const uint8_t* __restrict__ a, int64_t na,
+                                                               const uint8_t* __restrict__ b, int64_t nb,
+                                                               uint4* __restrict__ dst, int32_t* flags) {
+  __shared__ __align__(128) uint8_t ring[kWidenStages][kWidenChunk];
+  __shared__ uint64_t full[kWidenStages];
+  const int64_t ca = (na + kWidenChunk - 1) / kWidenChunk, cb = (nb + kWidenChunk - 1) / kWidenChunk;
+  const int64_t chunks = ca + cb;
+  // chunk c: its source, bytes and first output unit
+  auto chunk = [&](int64_t c, const uint8_t*& src, uint32_t& bytes, int64_t& unit0) {
+    const bool in_a = c < ca;
+    const int64_t off = (in_a ? c : c - ca) * kWidenChunk, total = in_a ? na : nb;
+    src = (in_a ? a : b) + off;
+    bytes = (uint32_t)(total - off < kWidenChunk ? total - off : kWidenChunk);
+    unit0 = ((in_a ? 0 : na) + off) / 8;
+  };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWidenStages; ++s) async::mbar_init(&full[s], 1);
+    async::fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t pol = async::policy_evict_first();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWidenStages; ++s) {
+      const int64_t c = blockIdx.x + (int64_t)s * gridDim.x;
+      if (c >= chunks) break;
+      const uint8_t* src;
+      uint32_t bytes;
+      int64_t unit0;
+      chunk(c, src, bytes, unit0);
+      async::mbar_expect_tx(&full[s], bytes);
+      async::bulk_g2s_hint(ring[s], src, bytes, &full[s], pol);
+    }
+  }
+  int it = 0;
+  bool ok = true;
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it) {
+    const int s = it % kWidenStages;
+    ok = async::mbar_wait_bounded(&full[s], (uint32_t)(it / kWidenStages) & 1u, 1000000000ull);
+    if (__syncthreads_or(!ok)) break;
+    const uint8_t* src;
+    uint32_t bytes;
+    int64_t unit0;
+    chunk(c, src, bytes, unit0);
+    const int units = (int)(bytes / 8);
+#pragma unroll 4
+    for (int u = threadIdx.x; u < units; u += kWidenThreads) {
+      const uint2 v = *reinterpret_cast<const uint2*>(ring[s] + u * 8);
+      const uint32_t w0 = v.x ^ 0x80808080u, w1 = v.y ^ 0x80808080u;
+      uint32_t h[4];
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[0]) : "r"(__byte_perm(w0, 0x64646464u, 0x4140)), "r"(0x64806480u));
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[1]) : "r"(__byte_perm(w0, 0x64646464u, 0x4342)), "r"(0x64806480u));
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[2]) : "r"(__byte_perm(w1, 0x64646464u, 0x4140)), "r"(0x64806480u));
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[3]) : "r"(__byte_perm(w1, 0x64646464u, 0x4342)), "r"(0x64806480u));
+      st16(dst + unit0 + u, make_uint4(h[0], h[1], h[2], h[3]));
+    }
+    __syncthreads();  // the buffer is read: refill it with the chunk kWidenStages steps ahead
+    if (threadIdx.x == 0) {
+      const int64_t cn = c + (int64_t)kWidenStages * gridDim.x;
+      if (cn < chunks) {
+        const uint8_t* srcn;
+        uint32_t bytesn;
+        int64_t unitn;
+        chunk(cn, srcn, bytesn, unitn);
+        async::mbar_expect_tx(&full[s], bytesn);
+        async::bulk_g2s_hint(ring[s], srcn, bytesn, &full[s], pol);
+      }
+    }
+  }
+  if (!ok && threadIdx.x == 0) {
+    raise_flag(flags, SQ_FLAG_TIMEOUT);
+    // let the copies this block issued land before its shared memory goes
+    for (int k2 = 0; k2 < kWidenStages; ++k2) {
+      const int j = it + k2;
+      if (blockIdx.x + (int64_t)j * gridDim.x >= chunks) break;
+      async::mbar_wait_bounded(&full[j % kWidenStages], (uint32_t)(j / kWidenStages) & 1u, 10000000ull);
+    }
+  }
+}
+
+// Bytes of workspace the widened operands take (X then W, fp16).
+size_t gemm_widen_bytes(int64_t m, int64_t n, int64_t k) { return (size_t)(m + n) * (size_t)k * 2; }
+
+// 1-byte codes through the tensor cores: both operands widened into the
+// workspace (one pass over the codes), then the fp16 form of the GEMM.
+sq_status gemm_i8_widened_tc(const void* xq, const float* x_scale, const void* wq, const float* w_scale,
+                             int64_t m, int64_t n, int64_t k, void* y, int32_t* acc_out, int32_t* flags,
+                             void* workspace, uint64_t wait_ns, int stall, cudaStream_t st) {
+  // bytes of codes: m * k and n * k, multiples of 16 (k % 16 == 0)
+  uint4* dst = static_cast<uint4*>(workspace);
+  const int64_t chunks = (m * k + kWidenChunk - 1) / kWidenChunk + (n * k + kWidenChunk - 1) / kWidenChunk;
+  const int64_t blocks = std::min<int64_t>(chunks, (int64_t)sm_count() * 4);
+  k_widen_codes<<<(unsigned)blocks, kWidenThreads, 0, st>>>(static_cast<const uint8_t*>(xq), m * k,
+                                                            static_cast<const uint8_t*>(wq), n * k, dst,
+                                                            flags);
+  const sq_status r = launch_status();
+  if (r != SQ_OK) return r;
+  const uint8_t* xw = static_cast<const uint8_t*>(workspace);
+  return gemm_bf16c_tc(xw, x_scale, xw + (size_t)m * (size_t)k * 2, w_scale, m, n, k, y, acc_out, flags,
+                       wait_ns, stall, st, true);
 }
 
 }  // namespace sq

@@ -67,6 +67,13 @@ SQ_DEVINL uint4 ld_stream16(const void* p) {
   return v;
 }
 
+// 8-byte streaming load that bypasses L1 allocation (read-once data).
+SQ_DEVINL uint2 ld_stream8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 // 16-byte load through the read-only path (reused data such as s_inv).
 SQ_DEVINL uint4 ld_ro16(const void* p) {
   uint4 v;

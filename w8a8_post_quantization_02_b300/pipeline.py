@@ -185,7 +185,7 @@ class Layer:
             "quant_act_static": sq.kernel_count(sq.SQ_OP_QUANT_ACT_STATIC, dt, T, 0, K, K),
             "fold_norm_gain": sq.kernel_count(sq.SQ_OP_FOLD_NORM_GAIN, dt, 0, 0, K),
             "rmsnorm_quant_act": sq.kernel_count(sq.SQ_OP_RMSNORM_QUANT_ACT, dt, T, 0, K, K),
-            "gemm": sq.kernel_count(sq.SQ_OP_GEMM, dt, T, N, K),
+            "gemm": sq.kernel_count(sq.SQ_OP_GEMM, dt, T, N, K, 0, sq._codes_fmt(self.codes)),
         }
 
     def kernel_count(self) -> int:
