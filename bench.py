@@ -268,8 +268,8 @@ def to_device(case, torch):
 NCU_TRAFFIC_BYTES = {
     # 107.96 MB read + 26.16 MB written (the rest of Y still dirty in L2)
     ("k_gemm_bf16c", "prefill_upgate_2048x4096x11008"): 134.12e6,
-    # 107.88 MB read (the widened fp16 operands) + 23.36 MB written
-    ("k_gemm_bf16c<fp16>", "prefill_upgate_2048x4096x11008"): 131.24e6,
+    # 107.91 MB read (the widened fp16 operands) + 23.49 MB written
+    ("k_gemm_bf16c<fp16>", "prefill_upgate_2048x4096x11008"): 131.40e6,
     # 16.88 MB read (the int8 weight codes and X codes), nothing written back yet
     ("k_gemm_dec", "decode_7b_16x4096x4096"): 16.88e6,
 }
