@@ -394,6 +394,9 @@ sq_status sq_channel_stats(const float* amax, const float* scale, int64_t n, dou
  *           [tokens x cin] codes in format fmt; w_scale fp32 [cout];
  *           x_scale fp32 [tokens]; y bf16 [tokens x cout]; workspace of at
  *           least sq_workspace_bytes(SQ_OP_FOLD_QUANTIZE, 0, cout, cin, fmt)
+ *           (steps 3 and 5 use it in turn: with sq_workspace_bytes(SQ_OP_GEMM,
+ *           tokens, cout, cin, fmt) bytes as well, step 5 takes its widening
+ *           path for 1-byte codes)
  *   dev_flags  device int32 or NULL, as in the steps
  * The copies are asynchronous only from page-locked host memory
  * (cudaHostAlloc or cudaHostRegister); from pageable memory CUDA stages them

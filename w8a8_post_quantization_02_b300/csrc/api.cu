@@ -400,8 +400,9 @@ sq_status sq_linear_host(const void* x_host, const void* w_host, sq_dtype dt, in
   if ((r = sq_quant_act(b.x, dt, tokens, cin, cin, b.s_inv, b.xq, fmt, b.x_scale, dev_flags,
                         stream)) != SQ_OK)
     return r;
+  // the fold is done with the workspace (same stream): the GEMM may reuse it
   if ((r = sq_w8a8_gemm(b.xq, b.x_scale, b.wq, b.w_scale, fmt, tokens, cout, cin, b.y, nullptr,
-                        dev_flags, nullptr, 0, stream)) != SQ_OK)
+                        dev_flags, b.workspace, b.ws_bytes, stream)) != SQ_OK)
     return r;
   if (cudaMemcpyAsync(y_host, b.y, (size_t)tokens * cout * 2, cudaMemcpyDeviceToHost, stream) !=
       cudaSuccess)

@@ -196,7 +196,10 @@ class Layer:
     def linear_buffers(self) -> "sq.LinearBuffers":
         """This layer's device buffers as the C ABI's sq_linear_buffers."""
         names = ("x", "w", "amax_x", "amax_w", "s", "s_inv", "wq", "w_scale", "xq", "x_scale", "y")
-        return sq.linear_buffers({n: getattr(self, n) for n in names}, self.ws_fold)
+        # the fold and the GEMM run one after the other on the call's stream:
+        # one buffer, the larger of the two workspaces, serves both
+        ws = self.ws_gemm if self.ws_gemm.numel() > self.ws_fold.numel() else self.ws_fold
+        return sq.linear_buffers({n: getattr(self, n) for n in names}, ws)
 
     def run_host(self, x_host: torch.Tensor, w_host: torch.Tensor, y_host: torch.Tensor,
                  stream=None, bufs: "sq.LinearBuffers | None" = None) -> None:
