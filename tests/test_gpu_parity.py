@@ -562,10 +562,13 @@ def test_full_workload_parity(sq, name, codes):
 
 # ------------------------------------------------------------------ whole path from host memory
 @pytest.mark.parametrize("name,codes", [("single_linear_64x512x512", None), ("decode_7b_16x4096x4096", None),
-                                        ("decode_7b_16x4096x4096", "bf16")])
+                                        ("decode_7b_16x4096x4096", "bf16"),
+                                        ("prefill_upgate_2048x4096x11008", "i8")])
 def test_linear_host_parity(sq, name, codes):
     """sq_linear_host: pinned host X and W in, host Y out, through the C ABI;
-    every intermediate bit-exact against the oracle, Y within 1 bf16 ulp."""
+    every intermediate bit-exact against the oracle, Y within 1 bf16 ulp.
+    The prefill case with 1-byte codes has the fold and the GEMM share one
+    workspace large enough for the GEMM's widened operands."""
     from w8a8_post_quantization_02_b300 import pipeline
     c = synth.workload(name)
     ref_ax = O.calibrate_absmax(c.x_f32(), 0)
