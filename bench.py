@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--codes", choices=["auto", "i8", "bf16"], default="auto",
                     help="storage of the INT8 codes: one byte each (i8), the same integers as exact "
-                         "bf16 values (bf16), or the library's choice for the token count (auto)")
+                         "bf16 values (bf16), or the library's choice (auto: one byte each)")
     ap.add_argument("--act-scale", choices=["dynamic", "static", "norm"], default="dynamic",
                     help="per-token scales (default), one calibrated scale per tensor, or per-token "
                          "scales after an RMS normalization whose gain absorbs S^-1 (the workload's X "
