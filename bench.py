@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--codes", choices=["auto", "i8", "bf16"], default="auto",
                     help="storage of the INT8 codes: one byte each (i8), the same integers as exact "
                          "bf16 values (bf16), or the library's choice (auto: one byte each)")
+    ap.add_argument("--i8-gemm", choices=["widened", "onchip"], default="widened",
+                    help="1-byte codes above 64 tokens: widen both operands to fp16 in the GEMM's "
+                         "workspace first (widened), or give the GEMM no workspace so it widens the "
+                         "codes in shared memory as it goes (onchip)")
     ap.add_argument("--act-scale", choices=["dynamic", "static", "norm"], default="dynamic",
                     help="per-token scales (default), one calibrated scale per tensor, or per-token "
                          "scales after an RMS normalization whose gain absorbs S^-1 (the workload's X "
@@ -270,6 +274,8 @@ NCU_TRAFFIC_BYTES = {
     ("k_gemm_bf16c", "prefill_upgate_2048x4096x11008"): 134.12e6,
     # 107.91 MB read (the widened fp16 operands) + 23.49 MB written
     ("k_gemm_bf16c<fp16>", "prefill_upgate_2048x4096x11008"): 131.40e6,
+    # (--i8-gemm onchip) 53.87 MB read (the int8 codes of X and W, once) + 9.99 MB written
+    ("k_gemm_i8c", "prefill_upgate_2048x4096x11008"): 63.86e6,
     # 16.88 MB read (the int8 weight codes and X codes), nothing written back yet
     ("k_gemm_dec", "decode_7b_16x4096x4096"): 16.88e6,
 }
@@ -285,7 +291,7 @@ def run_ours(args, case_name):
     case = synth.workload(case_name)
     x_host, w_host = to_device(case, torch)
     layer = pipeline.Layer.for_case(case, codes=None if args.codes == "auto" else args.codes,
-                                    act_scale=args.act_scale)
+                                    act_scale=args.act_scale, gemm_workspace=args.i8_gemm == "widened")
     layer.load(x_host.cuda(), w_host.cuda())
     stream = torch.cuda.current_stream()
     st = sq._stream(stream)
@@ -377,6 +383,8 @@ def run_ours(args, case_name):
     if layer.codes == "bf16" or layer.tokens > pipeline.I8_TENSOR_MIN_TOKENS:
         if layer.codes == "bf16":
             kern, what = "k_gemm_bf16c", "tcgen05 kind::f16 on bf16-coded int8"
+        elif not layer.gemm_workspace:
+            kern, what = "k_gemm_i8c", "int8 codes widened to fp16 on chip, tcgen05 kind::f16"
         else:
             # the timed GEMM call is two kernels: k_widen_codes (the codes to
             # fp16 in the workspace, ~23 us here) and the fp16 form of the GEMM
@@ -402,7 +410,9 @@ def run_ours(args, case_name):
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "s8", "data": "synthetic",
-        "config": dict(workload_config(case, layer.codes), act_scale=args.act_scale),
+        "config": dict(workload_config(case, layer.codes), act_scale=args.act_scale,
+                       **({"i8_gemm": args.i8_gemm}
+                          if layer.codes == "i8" and layer.tokens > pipeline.I8_TENSOR_MIN_TOKENS else {})),
         "gemm_tops": gemm_tops,
         "act_quant_gbs": iso[act_stage]["gbs"],
         "act_quant_hbm_frac": iso[act_stage]["hbm_frac"],
@@ -414,7 +424,8 @@ def run_ours(args, case_name):
     }
     if not args.no_e2e:
         if args.act_scale == "dynamic":
-            layers = [layer, pipeline.Layer.for_case(case, codes=layer.codes)]
+            layers = [layer, pipeline.Layer.for_case(case, codes=layer.codes,
+                                                     gemm_workspace=layer.gemm_workspace)]
             line["e2e"] = run_e2e(layers, x_host, w_host, args.e2e_steps, ops, world, torch)
     if rank == 0 and not args.no_cpu_baseline:
         nt = min(case.tokens, 256)

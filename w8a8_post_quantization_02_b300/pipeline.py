@@ -32,7 +32,8 @@ def choose_codes(tokens: int) -> str:
 
 class Layer:
     def __init__(self, tokens: int, cin: int, cout: int, dtype: str, alpha: float,
-                 codes: str | None = None, device="cuda", act_scale: str = "dynamic"):
+                 codes: str | None = None, device="cuda", act_scale: str = "dynamic",
+                 gemm_workspace: bool = True):
         if act_scale not in ("dynamic", "static", "norm"):
             raise ValueError("act_scale is 'dynamic' (per token), 'static' (one calibrated scale) or "
                              "'norm' (RMS normalization with S^-1 folded into its gain, then per token)")
@@ -66,15 +67,19 @@ class Layer:
         fmt = sq._codes_fmt(self.codes)
         self._fmt = fmt
         ws_fold = sq.workspace_bytes(sq.SQ_OP_FOLD_QUANTIZE, 0, cout, cin, self.codes)
-        ws_gemm = sq.workspace_bytes(sq.SQ_OP_GEMM, tokens, cout, cin, self.codes)
+        # without the GEMM's workspace, 1-byte codes above 64 tokens run the
+        # kernel that widens them in shared memory as it goes
+        ws_gemm = sq.workspace_bytes(sq.SQ_OP_GEMM, tokens, cout, cin, self.codes) if gemm_workspace else 0
+        self.gemm_workspace = bool(gemm_workspace)
         self.ws_fold = torch.empty(max(ws_fold, 256), dtype=torch.uint8, device=dv)
         self.ws_gemm = torch.empty(max(ws_gemm, 256), dtype=torch.uint8, device=dv)
         self._lib = sq.load_library()
 
     @classmethod
-    def for_case(cls, case, codes: str | None = None, act_scale: str = "dynamic") -> "Layer":
+    def for_case(cls, case, codes: str | None = None, act_scale: str = "dynamic",
+                 gemm_workspace: bool = True) -> "Layer":
         return cls(case.tokens, case.cin, case.cout, case.dtype, case.alpha, codes,
-                   act_scale=act_scale)
+                   act_scale=act_scale, gemm_workspace=gemm_workspace)
 
     def load(self, x: torch.Tensor, w: torch.Tensor) -> None:
         self.x.copy_(x)
@@ -187,7 +192,10 @@ class Layer:
             "quant_act_static": sq.kernel_count(sq.SQ_OP_QUANT_ACT_STATIC, dt, T, 0, K, K),
             "fold_norm_gain": sq.kernel_count(sq.SQ_OP_FOLD_NORM_GAIN, dt, 0, 0, K),
             "rmsnorm_quant_act": sq.kernel_count(sq.SQ_OP_RMSNORM_QUANT_ACT, dt, T, 0, K, K),
-            "gemm": sq.kernel_count(sq.SQ_OP_GEMM, dt, T, N, K, 0, sq._codes_fmt(self.codes)),
+            # the library counts with the workspace it asks for; without it the
+            # 1-byte GEMM is its one on-chip-widening kernel
+            "gemm": (sq.kernel_count(sq.SQ_OP_GEMM, dt, T, N, K, 0, sq._codes_fmt(self.codes))
+                     if self.gemm_workspace else 1),
         }
 
     def kernel_count(self) -> int:
