@@ -471,6 +471,9 @@ sq_status sq_read_device_flags(int32_t* dev_flags, int clear, int32_t* flags_out
  *   sq_test_w8a8_gemm_stalled: the kernel sq_w8a8_gemm would run for these
  *     arguments (SQ_ERR_UNSUPPORTED for the one GEMM kernel without pipeline
  *     waits: 1-byte codes with 17 to 64 tokens).
+ *   sq_test_w8a8_gemm_stalled_ws: the same with a workspace, so 1-byte codes
+ *     above 64 tokens take the widening path; its widening pass and its
+ *     GEMM both run stalled.
  *   sq_test_quant_act_stalled: the kernel of sq_quant_act.
  * dev_flags is required; 1e5 <= wait_ns <= 1e9 (else SQ_ERR_INVALID_ARG).
  * Other arguments as the product entry points.
@@ -479,6 +482,10 @@ sq_status sq_test_w8a8_gemm_stalled(const void* xq, const float* x_scale, const 
                                     const float* w_scale, sq_codes fmt, int64_t m, int64_t n,
                                     int64_t k, void* y, int32_t* dev_flags, uint64_t wait_ns,
                                     cudaStream_t stream);
+sq_status sq_test_w8a8_gemm_stalled_ws(const void* xq, const float* x_scale, const void* wq,
+                                       const float* w_scale, sq_codes fmt, int64_t m, int64_t n,
+                                       int64_t k, void* y, int32_t* dev_flags, void* workspace,
+                                       size_t ws_bytes, uint64_t wait_ns, cudaStream_t stream);
 sq_status sq_test_quant_act_stalled(const void* x, sq_dtype dt, int64_t tokens, int64_t cin,
                                     int64_t ldx, const float* s_inv, void* xq, sq_codes fmt,
                                     float* x_scale, int32_t* dev_flags, uint64_t wait_ns,

@@ -78,6 +78,37 @@ def test_gemm_wait_runs_out_then_recovers(sq, m, n, k, codes):
     assert sq.read_device_flags(flags) == (sq.SQ_OK, 0)
 
 
+@pytest.mark.parametrize("m,n,k", [(100, 264, 1024), (300, 512, 2048)])
+def test_widened_gemm_wait_runs_out_then_recovers(sq, m, n, k):
+    """1-byte codes with the GEMM's workspace: the widening pass and the fp16
+    GEMM after it both run stalled, both waits run out, and the product
+    call right after is exact."""
+    xq_np, wq_np = _codes(m, n, k, seed=m + 2 * n + k)
+    xs_np = (0.001 + synth.uniform(1, 8, m)).astype(F32)
+    ws_np = (0.0001 + synth.uniform(1, 9, n) * 0.01).astype(F32)
+    xq, wq = torch.from_numpy(xq_np).cuda(), torch.from_numpy(wq_np).cuda()
+    xs, ws = torch.from_numpy(xs_np).cuda(), torch.from_numpy(ws_np).cuda()
+    y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nbytes = sq.workspace_bytes(sq.SQ_OP_GEMM, m, n, k, "i8")
+    assert nbytes > 0
+    work = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    lib = sq.load_library()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    t0 = time.perf_counter()
+    st = lib.sq_test_w8a8_gemm_stalled_ws(P(xq), P(xs), P(wq), P(ws), sq.SQ_CODES_I8, m, n, k, P(y), P(flags),
+                                          P(work), nbytes, WAIT_NS, sq._stream())
+    assert st == sq.SQ_OK
+    status, word = sq.read_device_flags(flags, clear=True)
+    assert time.perf_counter() - t0 < 10.0
+    assert status == sq.SQ_ERR_TIMEOUT and word & sq.SQ_FLAG_TIMEOUT
+    y2, acc = sq.w8a8_gemm(xq, xs, wq, ws, want_acc=True, flags=flags, workspace=work)
+    ref_acc, ref_y = O.w8a8_gemm(xq_np, xs_np, wq_np, ws_np)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref_acc)
+    assert O.bf16_ulp_distance(y2.cpu().view(torch.int16).numpy().view(np.uint16), ref_y).max() <= 1
+    assert sq.read_device_flags(flags) == (sq.SQ_OK, 0)
+
+
 def test_quant_act_wait_runs_out_then_recovers(sq):
     c = synth.make_case("stall", 300, 4096, 8, dtype="bf16", outlier_frac=0.01, seed=9)
     si = (0.5 + synth.uniform(3, 4, 4096)).astype(F32)

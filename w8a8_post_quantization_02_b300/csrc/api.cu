@@ -346,6 +346,15 @@ sq_status sq_test_w8a8_gemm_stalled(const void* xq, const float* x_scale, const 
                             stream);
 }
 
+sq_status sq_test_w8a8_gemm_stalled_ws(const void* xq, const float* x_scale, const void* wq,
+                                       const float* w_scale, sq_codes fmt, int64_t m, int64_t n,
+                                       int64_t k, void* y, int32_t* dev_flags, void* workspace,
+                                       size_t ws_bytes, uint64_t wait_ns, cudaStream_t stream) {
+  if (!dev_flags || wait_ns < 100000ull || wait_ns > 1000000000ull) return SQ_ERR_INVALID_ARG;
+  return w8a8_gemm_dispatch(xq, x_scale, wq, w_scale, fmt, m, n, k, y, nullptr, dev_flags, wait_ns, 1,
+                            stream, workspace, ws_bytes);
+}
+
 sq_status sq_test_quant_act_stalled(const void* x, sq_dtype dt, int64_t tokens, int64_t cin,
                                     int64_t ldx, const float* s_inv, void* xq, sq_codes fmt,
                                     float* x_scale, int32_t* dev_flags, uint64_t wait_ns,

@@ -535,14 +535,16 @@ sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, co
 // block c mod gridDim.  One thread per block bulk-copies the block's chunks
 // into a ring of kWidenStages buffers; every thread widens 8-code units of
 // the current buffer and writes them to dst (16 bytes per unit, in order).
-// Every wait on the ring is bounded; one that runs out sets
-// SQ_FLAG_TIMEOUT and the block stops after its copies have landed.
+// Every wait on the ring is bounded (wait_ns); one that runs out sets
+// SQ_FLAG_TIMEOUT and the block stops after its copies have landed.  stall:
+// no copies are issued (the bounded waits' test; 0 on every product call).
 constexpr int kWidenThreads = 256;
 constexpr int kWidenChunk = 8192;
 constexpr int kWidenStages = 4;
 __global__ void __launch_bounds__(kWidenThreads) k_widen_codes(const uint8_t* __restrict__ a, int64_t na,
                                                                const uint8_t* __restrict__ b, int64_t nb,
-                                                               uint4* __restrict__ dst, int32_t* flags) {
+                                                               uint4* __restrict__ dst, int32_t* flags,
+                                                               uint64_t wait_ns, int stall) {
   __shared__ __align__(128) uint8_t ring[kWidenStages][kWidenChunk];
   __shared__ uint64_t full[kWidenStages];
   const int64_t ca = (na + kWidenChunk - 1) / kWidenChunk, cb = (nb + kWidenChunk - 1) / kWidenChunk;
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(kWidenThreads) k_widen_codes(const uint8_t* __
   }
   __syncthreads();
   const uint64_t pol = async::policy_evict_first();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !stall) {
     for (int s = 0; s < kWidenStages; ++s) {
       const int64_t c = blockIdx.x + (int64_t)s * gridDim.x;
       if (c >= chunks) break;
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(kWidenThreads) k_widen_codes(const uint8_t* __
   bool ok = true;
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it) {
     const int s = it % kWidenStages;
-    ok = async::mbar_wait_bounded(&full[s], (uint32_t)(it / kWidenStages) & 1u, 1000000000ull);
+    ok = async::mbar_wait_bounded(&full[s], (uint32_t)(it / kWidenStages) & 1u, wait_ns);
     if (__syncthreads_or(!ok)) break;
     const uint8_t* src;
     uint32_t bytes;
@@ -596,7 +598,7 @@ __global__ void __launch_bounds__(kWidenThreads) k_widen_codes(const uint8_t* __
       st16(dst + unit0 + u, make_uint4(h[0], h[1], h[2], h[3]));
     }
     __syncthreads();  // the buffer is read: refill it with the chunk kWidenStages steps ahead
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !stall) {
       const int64_t cn = c + (int64_t)kWidenStages * gridDim.x;
       if (cn < chunks) {
         const uint8_t* srcn;
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(kWidenThreads) k_widen_codes(const uint8_t* __
   if (!ok && threadIdx.x == 0) {
     raise_flag(flags, SQ_FLAG_TIMEOUT);
     // let the copies this block issued land before its shared memory goes
-    for (int k2 = 0; k2 < kWidenStages; ++k2) {
+    for (int k2 = 0; k2 < kWidenStages && !stall; ++k2) {
       const int j = it + k2;
       if (blockIdx.x + (int64_t)j * gridDim.x >= chunks) break;
       async::mbar_wait_bounded(&full[j % kWidenStages], (uint32_t)(j / kWidenStages) & 1u, 10000000ull);
@@ -633,7 +635,7 @@ sq_status gemm_i8_widened_tc(const void* xq, const float* x_scale, const void* w
   const int64_t blocks = std::min<int64_t>(chunks, (int64_t)sm_count() * 4);
   k_widen_codes<<<(unsigned)blocks, kWidenThreads, 0, st>>>(static_cast<const uint8_t*>(xq), m * k,
                                                             static_cast<const uint8_t*>(wq), n * k, dst,
-                                                            flags);
+                                                            flags, wait_ns, stall);
   const sq_status r = launch_status();
   if (r != SQ_OK) return r;
   const uint8_t* xw = static_cast<const uint8_t*>(workspace);

@@ -59,6 +59,8 @@ SIGNATURES = {
                               _P, _P]),
     "sq_read_device_flags": (_I32, [_P, _I32, ctypes.POINTER(ctypes.c_int32), _P]),
     "sq_test_w8a8_gemm_stalled": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, ctypes.c_uint64, _P]),
+    "sq_test_w8a8_gemm_stalled_ws": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _SZ,
+                                            ctypes.c_uint64, _P]),
     "sq_test_quant_act_stalled": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _I32, _P, _P, ctypes.c_uint64,
                                          _P]),
     "sq_status_string": (ctypes.c_char_p, [_I32]),
