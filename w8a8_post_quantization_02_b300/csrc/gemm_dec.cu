@@ -48,22 +48,13 @@ constexpr int kSmem = kWarps * kSlice + 2 * kWarps * 8 + 16 + 1024;
 static_assert(kThreads == 16 * kChan, "the epilogue maps threads onto 16 tokens x 32 channels");
 static_assert(kWBox % 1024 == 0 && kXBox % 1024 == 0, "boxes start on 128-byte-swizzle atoms");
 
-SQ_DEVINL uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // 16 int8 codes -> 8 registers of two exact fp16 values each (codes 2i and
-// 2i + 1 in register i): byte u = code + 128 as the fp16 pattern 0x6400 | u
-// is 1024 + u, minus 1152 exactly.
+// 2i + 1 in register i), by codes4_to_f16x2.
 SQ_DEVINL void codes_to_f16(uint4 v, uint32_t* h) {
-  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    h[2 * i] = hsub2(__byte_perm(w[i], 0x64646464u, 0x4140), 0x64806480u);
-    h[2 * i + 1] = hsub2(__byte_perm(w[i], 0x64646464u, 0x4342), 0x64806480u);
-  }
+  codes4_to_f16x2(v.x, h[0], h[1]);
+  codes4_to_f16x2(v.y, h[2], h[3]);
+  codes4_to_f16x2(v.z, h[4], h[5]);
+  codes4_to_f16x2(v.w, h[6], h[7]);
 }
 
 SQ_DEVINL void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,

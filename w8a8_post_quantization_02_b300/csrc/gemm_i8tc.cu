@@ -135,29 +135,14 @@ struct Problem {
   uint64_t wait_ns;  // bound on every pipeline wait
 };
 
-SQ_DEVINL uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // 16 int8 codes (one 16-byte vector, code k in byte k) -> the same 16
-// integers as exact fp16 values, elements 0-7 in `lo` and 8-15 in `hi`.
-// Flipping a byte's top bit gives u = code + 128 in [1, 255]; the fp16 bit
-// pattern 0x6400 | u is exactly 1024 + u; subtracting 1152 (0x6480) is exact
-// (both operands within a factor of two) and leaves the code.
+// integers as exact fp16 values, elements 0-7 in `lo` and 8-15 in `hi`
+// (codes4_to_f16x2 on each word).
 SQ_DEVINL void codes_to_f16(uint4 v, uint4& lo, uint4& hi) {
-  const uint32_t w0 = v.x ^ 0x80808080u, w1 = v.y ^ 0x80808080u;
-  const uint32_t w2 = v.z ^ 0x80808080u, w3 = v.w ^ 0x80808080u;
-  const uint32_t K64 = 0x64646464u, K1152 = 0x64806480u;
-  lo.x = hsub2(__byte_perm(w0, K64, 0x4140), K1152);
-  lo.y = hsub2(__byte_perm(w0, K64, 0x4342), K1152);
-  lo.z = hsub2(__byte_perm(w1, K64, 0x4140), K1152);
-  lo.w = hsub2(__byte_perm(w1, K64, 0x4342), K1152);
-  hi.x = hsub2(__byte_perm(w2, K64, 0x4140), K1152);
-  hi.y = hsub2(__byte_perm(w2, K64, 0x4342), K1152);
-  hi.z = hsub2(__byte_perm(w3, K64, 0x4140), K1152);
-  hi.w = hsub2(__byte_perm(w3, K64, 0x4342), K1152);
+  codes4_to_f16x2(v.x, lo.x, lo.y);
+  codes4_to_f16x2(v.y, lo.z, lo.w);
+  codes4_to_f16x2(v.z, hi.x, hi.y);
+  codes4_to_f16x2(v.w, hi.z, hi.w);
 }
 
 // Byte offset of 16-byte chunk j of row r in a K-major tile of 128-byte

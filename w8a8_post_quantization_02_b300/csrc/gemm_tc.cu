@@ -528,9 +528,7 @@ sq_status gemm_bf16c_tc(const void* xq, const float* x_scale, const void* wq, co
 #undef SQ_TC_LAUNCH
 }
 
-// 1-byte codes widened to exact fp16 values (flip the sign bit, place the
-// byte in the significand of 1024 + u, subtract 1152: every step exact).
-// The codes of a (na bytes) and then b (nb bytes) are cut into chunks of
+// 1-byte codes widened to exact fp16 values (codes4_to_f16x2).  The codes of a (na bytes) and then b (nb bytes) are cut into chunks of
 // kWidenChunk bytes (a's last chunk may be short, and b's); chunk c goes to
 // block c mod gridDim.  One thread per block bulk-copies the block's chunks
 // into a ring of kWidenStages buffers; every thread widens 8-code units of
@@ -589,12 +587,9 @@ __global__ void __launch_bounds__(kWidenThreads) k_widen_codes(const uint8_t* __
 #pragma unroll 4
     for (int u = threadIdx.x; u < units; u += kWidenThreads) {
       const uint2 v = *reinterpret_cast<const uint2*>(ring[s] + u * 8);
-      const uint32_t w0 = v.x ^ 0x80808080u, w1 = v.y ^ 0x80808080u;
       uint32_t h[4];
-      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[0]) : "r"(__byte_perm(w0, 0x64646464u, 0x4140)), "r"(0x64806480u));
-      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[1]) : "r"(__byte_perm(w0, 0x64646464u, 0x4342)), "r"(0x64806480u));
-      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[2]) : "r"(__byte_perm(w1, 0x64646464u, 0x4140)), "r"(0x64806480u));
-      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[3]) : "r"(__byte_perm(w1, 0x64646464u, 0x4342)), "r"(0x64806480u));
+      codes4_to_f16x2(v.x, h[0], h[1]);
+      codes4_to_f16x2(v.y, h[2], h[3]);
       st16(dst + unit0 + u, make_uint4(h[0], h[1], h[2], h[3]));
     }
     __syncthreads();  // the buffer is read: refill it with the chunk kWidenStages steps ahead

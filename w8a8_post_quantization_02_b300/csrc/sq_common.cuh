@@ -178,6 +178,18 @@ SQ_DEVINL uint32_t pack4_codes(float m0, float m1, float m2, float m3) {
   return __byte_perm(lo, hi, 0x5410);
 }
 
+// Four int8 codes (code k in byte k of w) -> the same four integers as
+// exact fp16 values: codes 0 and 1 in lo (code 0 in the low half), 2 and 3
+// in hi.  Flipping a byte's top bit gives u = code + 128 in [1, 255]; the
+// fp16 bit pattern 0x6400 | u is exactly 1024 + u; subtracting 1152
+// (0x6480) is exact (both operands within a factor of two) and leaves the
+// code.
+SQ_DEVINL void codes4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(__byte_perm(u, 0x64646464u, 0x4140)), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(__byte_perm(u, 0x64646464u, 0x4342)), "r"(0x64806480u));
+}
+
 SQ_DEVINL uint32_t pack2_bf16codes(float m0, float m1) {
   return magic_to_bf16bits(m0) | (magic_to_bf16bits(m1) << 16);
 }
