@@ -256,8 +256,11 @@ struct Layout {
 
 // One CTA of a CL-CTA cluster: rows [rank*R, rank*R + R) of the strip of
 // output channels [n0, n0 + SW).
-template <bool BF16, int CODES, int CL>
-__global__ void __launch_bounds__(kThreads) k_fold_strip(const __grid_constant__ CUtensorMap map_w,
+// MINB: 3 builds the kernel for three CTAs per SM (at most 80 registers,
+// a few bytes spilled), 0 leaves the compiler's choice (83-88 registers, so
+// two CTAs per SM).  See launch_cl for which runs.
+template <bool BF16, int CODES, int CL, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) k_fold_strip(const __grid_constant__ CUtensorMap map_w,
                                                          const float* __restrict__ s, int64_t cin,
                                                          int64_t cout, int rows_per_cta,
                                                          uint8_t* __restrict__ wq,
@@ -453,11 +456,11 @@ int64_t rows_per_cta(int64_t cin, int cl) {
   return (r + kBoxRows - 1) / kBoxRows * kBoxRows;
 }
 
-template <bool BF16, int CODES, int CL>
+template <bool BF16, int CODES, int CL, int MINB>
 sq_status launch(const CUtensorMap& map, const float* s, int64_t cin, int64_t cout, int rpc,
                  uint8_t* wq, float* w_scale, int32_t* flags, cudaStream_t st) {
   constexpr int EPC = BF16 ? 8 : 4;
-  auto kern = k_fold_strip<BF16, CODES, CL>;
+  auto kern = k_fold_strip<BF16, CODES, CL, MINB>;
   const size_t smem = Layout<EPC>(rpc).total + 1024;
   static std::atomic<uint64_t> attr_done{0};
   if (!once_per_device(attr_done, [&] {
@@ -485,15 +488,31 @@ sq_status launch(const CUtensorMap& map, const float* s, int64_t cin, int64_t co
   return launch_status();
 }
 
+template <bool BF16, int CODES, int MINB>
+sq_status launch_cl_b(int cl, const CUtensorMap& map, const float* s, int64_t cin, int64_t cout,
+                      int rpc, uint8_t* wq, float* w_scale, int32_t* flags, cudaStream_t st) {
+  switch (cl) {
+    case 1: return launch<BF16, CODES, 1, MINB>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+    case 2: return launch<BF16, CODES, 2, MINB>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+    case 4: return launch<BF16, CODES, 4, MINB>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+    default: return launch<BF16, CODES, 8, MINB>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
+  }
+}
+
+// The three-CTA build where shared memory lets three CTAs share an SM (at
+// most 1024 rows per CTA) and the grid holds at least two such waves.
+// Measured on B300 (bf16 W, 1-byte codes): 4096 x 11008 54.5 -> 51.1 us,
+// 8192 x 10240 98.7 -> 87.5 us (bf16 codes 60.7 -> 53.8, 110 -> 96); the
+// 4096 x 4096 decode weight (512 CTAs) and CTAs of 1408 rows (two per SM by
+// shared memory) were slower with it (25.2 -> 28.4, 60.1 -> 62.6 us).
 template <bool BF16, int CODES>
 sq_status launch_cl(int cl, const CUtensorMap& map, const float* s, int64_t cin, int64_t cout,
                     int rpc, uint8_t* wq, float* w_scale, int32_t* flags, cudaStream_t st) {
-  switch (cl) {
-    case 1: return launch<BF16, CODES, 1>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
-    case 2: return launch<BF16, CODES, 2>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
-    case 4: return launch<BF16, CODES, 4>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
-    default: return launch<BF16, CODES, 8>(map, s, cin, cout, rpc, wq, w_scale, flags, st);
-  }
+  constexpr int EPC = BF16 ? 8 : 4;
+  const int64_t ctas = (cout + 4 * EPC - 1) / (4 * EPC) * cl;
+  if (rpc <= 1024 && ctas >= 2 * 3 * (int64_t)sm_count())
+    return launch_cl_b<BF16, CODES, 3>(cl, map, s, cin, cout, rpc, wq, w_scale, flags, st);
+  return launch_cl_b<BF16, CODES, 0>(cl, map, s, cin, cout, rpc, wq, w_scale, flags, st);
 }
 
 int cluster_size(int64_t cin) {
