@@ -791,6 +791,64 @@ def test_rmsnorm_fold_bit_exact(sq, tokens, cin, dtype, codes):
     assert np.array_equal(codes_np(xq), q_ref)
 
 
+def _exact_bf16_bits(v) -> np.ndarray:
+    """bf16 bit patterns of values that bf16 holds exactly (subnormals too)."""
+    b = np.asarray(v, np.float64).astype(F32).view(np.uint32)
+    assert not np.any(b & 0xFFFF)
+    return (b >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("cin", [64, 4096, 8192])
+def test_rmsnorm_sum_boundaries(sq, cin, dtype):
+    """Sums of squares on and next to binary32 midpoints, and rows whose
+    threads hold values far apart or at the ends of the exponent range:
+    - 1 + 2^-24 exactly (a tie: even, so 1);
+    - 1 + 2^-24 + 2^-56 (just above the tie);
+    - 1 + 2^-24 + 2^-120 (a square 2^96 times below the others' unit);
+    - a 2^62 value in one thread and 2^-60-sized values in another;
+    - rows of 2^-56-sized and 2^40-sized values, one with 1.5 * 2^60 and one
+      with 1.5 * 2^61 in its first thread;
+    - 1.5 with a 2^-100 value and the bf16 subnormal 2^-130 beside it.
+    The scale and the codes must equal the exact-sum oracle's."""
+    rng = np.random.default_rng(cin + (7 if dtype == "bf16" else 0))
+    rows = np.zeros((10, cin), np.float64)
+    rows[0, :2] = [1.0, 2.0 ** -12]
+    rows[1, :3] = [1.0, 2.0 ** -12, 2.0 ** -28]
+    rows[2, :3] = [1.0, 2.0 ** -12, 2.0 ** -60]
+    base = np.round(rng.standard_normal((7, cin)) * 16) / 16   # at most 8 significant bits: exact in bf16
+    rows[3] = base[0]
+    rows[3, 8] = 2.0 ** 62
+    rows[3, 16:24] = base[1, :8] * 2.0 ** -60
+    rows[4] = base[2] * 2.0 ** -56
+    rows[5] = base[3] * 2.0 ** 40
+    rows[5, 0] = 1.5 * 2.0 ** 60
+    rows[6] = base[4] * 2.0 ** 40
+    rows[6, 0] = 1.5 * 2.0 ** 61
+    rows[7] = base[5]
+    rows[7, :3] = [1.5, 2.0 ** -100, 2.0 ** -130]
+    rows[8] = base[6]
+    rows[9, :3] = [1.0, 2.0 ** -12, -(2.0 ** -60)]
+    if dtype == "bf16":
+        h = _exact_bf16_bits(rows)
+        hf = synth.bf16_bits_to_f32(h)
+    else:
+        h = rows.astype(F32)
+        assert np.array_equal(h.astype(np.float64), rows)
+        hf = h
+    gamma = np.ones(cin, F32)
+    eps = 1e-5
+    q_ref, xs_ref, nf = O.rmsnorm_quant_act(hf, gamma, eps)
+    assert not nf
+    assert O.sum_squares_f32(hf[0]) == F32(1.0)
+    assert O.sum_squares_f32(hf[1]) == O.sum_squares_f32(hf[2]) == F32(1.0 + 2.0 ** -23)
+    flags = flags_tensor()
+    xq, xs = sq.rmsnorm_quant_act(dev(h, dtype), torch.from_numpy(gamma).cuda(), eps, "i8", flags)
+    assert int(flags.item()) == 0
+    assert np.array_equal(f32bits(xs), npbits(xs_ref))
+    assert np.array_equal(codes_np(xq), q_ref)
+
+
 def test_rmsnorm_nonfinite_flag(sq):
     h = torch.ones(4, 64, device="cuda")
     h[2, 9] = float("inf")

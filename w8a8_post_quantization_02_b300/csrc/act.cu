@@ -64,6 +64,10 @@ constexpr int kDynamic = 0;  // per-token scale from the row's max|X'|
 constexpr int kStatic = 1;   // one calibrated scale for every token
 constexpr int kNorm = 2;     // RMS normalization with the folded gain, then per-token scale
 
+// Flag bits beside a warp's exponent in the kNorm exchange: bits were
+// dropped below the unit; a thread of the warp used the fast sum.
+constexpr uint32_t kStickyBit = 1u << 16, kFastBit = 1u << 17;
+
 // 128-bit unsigned integer as (hi, lo).
 struct U128 {
   uint64_t hi, lo;
@@ -74,21 +78,31 @@ SQ_DEVINL U128 add128(U128 a, U128 b) {
   r.hi = a.hi + b.hi + (r.lo < a.lo ? 1ull : 0ull);
   return r;
 }
+SQ_DEVINL U128 sub128(U128 a, U128 b) {  // a - b, a >= b
+  U128 r;
+  r.lo = a.lo - b.lo;
+  r.hi = a.hi - b.hi - (a.lo < b.lo ? 1ull : 0ull);
+  return r;
+}
 
 // Exact sums of squares as 128-bit fixed-point integers.  For h with
 // binary32 exponent field e (>= 1 after subnormals) and 24-bit significand
 // m, h^2 = m^2 * 2^(2e - 300).  A partial sum relative to exponent E holds
 // I = sum m^2 * 2^(62 - 2 (E - e)), i.e. sum h^2 = I * 2^(2E - 362); every
-// term is below 2^110, so a row of 32768 terms stays below 2^125.  Terms
-// more than 2^62 below the largest are truncated at the unit (relative
-// error below 2^-95: far under float64 resolution).
-SQ_DEVINL U128 shl128(uint64_t v, int sh) {  // v * 2^sh truncated, v < 2^48, sh <= 62
+// term is below 2^110, so a row of 32768 terms stays below 2^125.  Bits of
+// a term more than 2^62 below the largest fall below the unit: they are
+// dropped, and `sticky` records that a nonzero part was dropped, so that a
+// sum that would otherwise sit exactly on a binary32 midpoint is known to
+// lie above it.
+SQ_DEVINL U128 shl128(uint64_t v, int sh, bool& sticky) {  // v * 2^sh, v < 2^48, sh <= 62
   U128 r;
   if (sh >= 0) {
     r.lo = v << sh;
     r.hi = sh ? (v >> (64 - sh)) : 0ull;
   } else {
-    r.lo = (-sh < 64) ? (v >> (-sh)) : 0ull;
+    const int k = -sh;
+    sticky |= (k < 64 ? (v & ((1ull << k) - 1ull)) : v) != 0ull;
+    r.lo = k < 64 ? (v >> k) : 0ull;
     r.hi = 0ull;
   }
   return r;
@@ -109,11 +123,25 @@ SQ_DEVINL U128 shr128(U128 x, int sh) {  // x / 2^sh truncated, sh >= 0
   return r;
 }
 
+// The same, recording in `sticky` whether nonzero bits were shifted out.
+SQ_DEVINL U128 shr128(U128 x, int sh, bool& sticky) {
+  if (sh == 0) return x;
+  bool lost;
+  if (sh >= 128)
+    lost = (x.hi | x.lo) != 0ull;
+  else if (sh >= 64)
+    lost = x.lo != 0ull || (sh > 64 && (x.hi & ((1ull << (sh - 64)) - 1ull)) != 0ull);
+  else
+    lost = (x.lo & ((1ull << sh) - 1ull)) != 0ull;
+  sticky |= lost;
+  return shr128(x, sh);
+}
+
 // Add h^2 for the element with |h| bits b to the sum I relative to exponent
 // E.  bf16-origin values (low 16 significand bits zero) within 2^15 of the
 // largest take a single 32 x 32 -> 64-bit multiply-add into the high word.
 template <bool BF16>
-SQ_DEVINL void add_square(U128& acc, uint32_t b, int E) {
+SQ_DEVINL void add_square(U128& acc, uint32_t b, int E, bool& sticky) {
   const int e = (int)(b >> 23);
   const int d2 = 2 * (E - (e ? e : 1));
   if constexpr (BF16) {
@@ -124,20 +152,23 @@ SQ_DEVINL void add_square(U128& acc, uint32_t b, int E) {
       acc.hi += add;
       return;
     }
-    acc = add128(acc, shl128((uint64_t)sq << 32, 62 - d2));
+    acc = add128(acc, shl128((uint64_t)sq << 32, 62 - d2, sticky));
   } else {
     const uint64_t m = (uint64_t)((b & 0x7FFFFFu) | (e ? 0x800000u : 0u));
-    acc = add128(acc, shl128(m * m, 62 - d2));
+    acc = add128(acc, shl128(m * m, 62 - d2, sticky));
   }
 }
 
 // I * 2^u rounded once to binary32 (nearest, ties to even; subnormal
-// results rounded at their own position, overflow to +inf).
-SQ_DEVINL float u128_scaled_to_f32(U128 x, int u) {
+// results rounded at their own position, overflow to +inf).  `sticky`: the
+// true value lies strictly above I * 2^u by less than one unit.
+SQ_DEVINL float u128_scaled_to_f32(U128 x, int u, bool sticky) {
   if (x.hi == 0 && x.lo == 0) return 0.0f;
   const int t = x.hi ? 127 - __clzll((long long)x.hi) : 63 - __clzll((long long)x.lo);  // top bit
   const int shift = max(t - 23, -149 - u);     // bits below `shift` are rounded off
-  if (shift <= 0) return ldexpf((float)x.lo, u);  // at most 24 significant bits: exact
+  // at most 24 significant bits: exact, and a sticky part below the unit is
+  // under half a unit of the result
+  if (shift <= 0) return ldexpf((float)x.lo, u);
   // the sums held here stay below 2^125, so a shift of 128 or more means a
   // value below 2^-152: under half the smallest subnormal
   if (shift >= 128) return 0.0f;
@@ -162,8 +193,98 @@ SQ_DEVINL float u128_scaled_to_f32(U128 x, int u) {
   }
   const bool gt = rem.hi > half.hi || (rem.hi == half.hi && rem.lo > half.lo);
   const bool eq = rem.hi == half.hi && rem.lo == half.lo;
-  if (gt || (eq && (q & 1u))) ++q;
+  if (gt || (eq && (sticky || (q & 1u)))) ++q;
   return ldexpf((float)q, shift + u);          // q <= 2^24: exact scaling
+}
+
+// Fast sum of squares of one thread's bf16-origin values, used when the
+// thread's largest exponent field et lies in [kFastLo, kFastHi].  With
+// U = 2^(2 (et - 127)) every square is below 4U.  Each square is split on
+// the grid 2^-16 U by an add of sigma = 192 U (hi = RN(h^2 + sigma) - sigma,
+// exact by Sterbenz's lemma) and lo = h^2 - hi (one fused multiply-add,
+// exact: a bf16 square has 16 significant bits).  The hi parts sum exactly
+// (multiples of 2^-16 U below 2^7 U); the lo parts, each at most 2^-17 U,
+// sum with rounding error below 2^-33 U for 32 values (two running sums of
+// 16, each add off by at most 2^-38 U, the last by 2^-37 U), and squares
+// below the normal range add at most 32 * 2^-150 <= 2^-35 U (U >= 2^-110).
+// So the result, returned in the fixed-point form relative to et (rounded
+// there at 2^-68 U), is within 2^-32.6 U of the thread's exact sum, and U is
+// at most its largest square.
+constexpr int kFastLo = 72, kFastHi = 187;
+template <int N>
+SQ_DEVINL U128 fast_sum_squares_bf16(const float* h, int et) {
+  static_assert(N % 2 == 0 && N <= 32, "at most 32 values, in pairs");
+  const float sigma = __uint_as_float(((uint32_t)(2 * et - 120) << 23) | 0x400000u);  // 192 U
+  float sh0 = 0.0f, sh1 = 0.0f, sl0 = 0.0f, sl1 = 0.0f;
+#pragma unroll
+  for (int k = 0; k < N; k += 2) {
+    float t0 = h[k], t1 = h[k + 1];
+    fma2_rn(t0, t1, h[k], h[k + 1], sigma, sigma);      // RN(h^2 + sigma)
+    add2_rn(t0, t1, -sigma, -sigma);                    // hi, exact
+    float l0 = h[k], l1 = h[k + 1];
+    fma2_rn(l0, l1, h[k], h[k + 1], -t0, -t1);          // lo = h^2 - hi, exact
+    add2_rn(sh0, sh1, t0, t1);
+    add2_rn(sl0, sl1, l0, l1);
+  }
+  const float s_hi = __fadd_rn(sh0, sh1);  // exact
+  const float s_lo = __fadd_rn(sl0, sl1);
+  // s_hi = H * 2^-16 U: H << 92 in units of 2^(2 et - 362)
+  const uint32_t H = __float2uint_rn(__fmul_rn(s_hi, __uint_as_float((uint32_t)(397 - 2 * et) << 23)));
+  // s_lo / U, then at the unit 2^-68 U (2^40 units): |L| <= 2^56
+  const long long L =
+      __float2ll_rn(__fmul_rn(__fmul_rn(s_lo, __uint_as_float((uint32_t)(381 - 2 * et) << 23)), 0x1p68f));
+  const U128 a = {(uint64_t)H << 28, 0ull};
+  const U128 b = {(uint64_t)(L >> 24), (uint64_t)L << 40};  // L * 2^40, two's complement
+  return add128(a, b);                                         // the sum is positive
+}
+
+// Exact sum of squares of one thread's values relative to exponent et.
+template <bool BF16, int N>
+SQ_DEVINL U128 exact_sum_squares(const float* h, int et, bool& sticky) {
+  U128 acc = {0ull, 0ull};
+#pragma unroll
+  for (int k = 0; k < N; ++k) add_square<BF16>(acc, __float_as_uint(h[k]) & 0x7FFFFFFFu, et, sticky);
+  return acc;
+}
+
+// Sum of a warp's 128-bit partial sums, each relative to its lane's exponent
+// et, aligned to the warp's largest exponent (returned in ew).
+SQ_DEVINL U128 warp_sum128(U128 acc, int et, int& ew, bool& sticky) {
+  ew = (int)__reduce_max_sync(0xFFFFFFFFu, (uint32_t)et);
+  acc = shr128(acc, 2 * (ew - et), sticky);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    U128 other;
+    other.hi = __shfl_xor_sync(0xFFFFFFFFu, acc.hi, o);
+    other.lo = __shfl_xor_sync(0xFFFFFFFFu, acc.lo, o);
+    acc = add128(acc, other);
+  }
+  return acc;
+}
+
+// Sum of the NW warps' partial sums (red_s, with exponents and flag bits in
+// red_e) in every warp: lane w aligns warp w's sum to the row's largest
+// exponent eb and a butterfly over the first NW lanes adds them (integer
+// sums: the order does not matter).  Returns the OR of the flag bits.
+template <int NW>
+SQ_DEVINL U128 block_sum128(const U128* red_s, const uint32_t* red_e, int lane, int& eb,
+                            uint32_t& bits) {
+  static_assert((NW & (NW - 1)) == 0 && NW <= 32, "power-of-two warp count");
+  const uint32_t re = lane < NW ? red_e[lane] : 1u;
+  const int ew_l = (int)(re & 0xFFFFu);
+  eb = (int)__reduce_max_sync(0xFFFFFFFFu, (uint32_t)ew_l);
+  bool sticky = false;
+  U128 tot = {0ull, 0ull};
+  if (lane < NW) tot = shr128(red_s[lane], 2 * (eb - ew_l), sticky);
+#pragma unroll
+  for (int o = NW / 2; o > 0; o >>= 1) {
+    U128 other;
+    other.hi = __shfl_xor_sync(0xFFFFFFFFu, tot.hi, o);
+    other.lo = __shfl_xor_sync(0xFFFFFFFFu, tot.lo, o);
+    tot = add128(tot, other);
+  }
+  bits = __reduce_or_sync(0xFFFFFFFFu, (re & ~0xFFFFu) | (sticky ? kStickyBit : 0u));
+  return tot;
 }
 
 // NT threads per CTA, each owning VPT 16-byte vectors of every row (vector
@@ -173,10 +294,13 @@ SQ_DEVINL float u128_scaled_to_f32(U128 x, int u) {
 // MODE kStatic: one calibrated scale *d_static for every token instead of
 // the row maximum (no reduction; the clamp can act and `clipped` counts it).
 // MODE kNorm: `s_inv` holds the folded gain gamma' and the row is first
-// RMS-normalized: the sum of squares is exact (128-bit fixed point,
-// order-independent) and rounded once to binary32, then
+// RMS-normalized: S, the exact sum of squares rounded once to binary32
+// (128-bit fixed point, order-independent; bf16 rows take a split sum on the
+// floating-point pipe whose error bound decides the rounding, and redo the
+// exact sum in the rare rows where it cannot), then
 // r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))) in IEEE binary32 and
-// X' = RN(RN(h * r) * gamma').  Two block barriers per row.
+// X' = RN(RN(h * r) * gamma').  Two block barriers per row (three when the
+// exact sum is redone).
 // From 512 threads up the kernel is built for one block per SM, which leaves
 // the compiler its full register budget (0 below: no minimum).  Measured on
 // B300: 2048 x 11008 bf16 24.7 -> 22.4 us (RMS-normalizing mode 70.2 ->
@@ -257,42 +381,46 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 1 : 0) k_quant_act(const uint8
     float p[VPT][E];
     float m = 0.0f;
     if constexpr (NORM) {
-      // the row into registers, the thread's largest binary32 exponent, and
-      // its exact sum of squares relative to that exponent
+      // the row into registers and the thread's largest binary32 exponent
       uint32_t tb = 0u;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = tid + i * NT;
         if (ok && v < nvec) {
-          unpack<BF16>(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), p[i]);
+          const uint4 raw = *reinterpret_cast<const uint4*>(buf + (size_t)v * 16);
+          unpack<BF16>(raw, p[i]);
+          if constexpr (BF16) {  // packed magnitudes, NaN kept (exponent 255)
+            tb = absmax_nan_bf16x2(tb, absmax_nan_bf16x2(absmax_nan_bf16x2(raw.x, raw.y),
+                                                         absmax_nan_bf16x2(raw.z, raw.w)));
+          } else {
 #pragma unroll
-          for (int e = 0; e < E; ++e) tb = max(tb, __float_as_uint(p[i][e]) & 0x7FFFFFFFu);
+            for (int e = 0; e < E; ++e) tb = max(tb, __float_as_uint(p[i][e]) & 0x7FFFFFFFu);
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < E; ++e) p[i][e] = 0.0f;
         }
       }
+      if constexpr (BF16) tb = max(tb & 0x7FFFu, (tb >> 16) & 0x7FFFu) << 16;
       const int et = max(1, (int)(tb >> 23));  // 255: a non-finite value
+      // the thread's sum of squares relative to et: the fast split sum for
+      // bf16 values in its exponent range (within 2^-31 U), else exact
+      bool fast = false;
+      if constexpr (BF16) fast = et >= kFastLo && et <= kFastHi;
+      bool sticky = false;
       U128 acc = {0ull, 0ull};
-      if (et < 255) {
-#pragma unroll
-        for (int i = 0; i < VPT; ++i)
-#pragma unroll
-          for (int e = 0; e < E; ++e) add_square<BF16>(acc, __float_as_uint(p[i][e]) & 0x7FFFFFFFu, et);
+      if (fast) {
+        if constexpr (BF16) acc = fast_sum_squares_bf16<VPT * E>(&p[0][0], et);
+      } else if (et < 255) {
+        acc = exact_sum_squares<BF16, VPT * E>(&p[0][0], et, sticky);
       }
-      // warp: align to the warp's largest exponent, then add (exact)
-      const int ew = (int)__reduce_max_sync(0xFFFFFFFFu, (uint32_t)et);
-      acc = shr128(acc, 2 * (ew - et));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        U128 other;
-        other.hi = __shfl_xor_sync(0xFFFFFFFFu, acc.hi, o);
-        other.lo = __shfl_xor_sync(0xFFFFFFFFu, acc.lo, o);
-        acc = add128(acc, other);
-      }
+      int ew;
+      acc = warp_sum128(acc, et, ew, sticky);
+      const uint32_t wbits = (__any_sync(0xFFFFFFFFu, sticky) ? kStickyBit : 0u) |
+                             (__any_sync(0xFFFFFFFFu, fast) ? kFastBit : 0u);
       if (lane == 0) {
         red_s[(it & 1) * NW + warp] = acc;
-        red_e[(it & 1) * NW + warp] = (uint32_t)ew;
+        red_e[(it & 1) * NW + warp] = (uint32_t)ew | wbits;
       }
       if (__syncthreads_or(!ok)) {
         aborted = true;
@@ -305,27 +433,54 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 1 : 0) k_quant_act(const uint8
           bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
         }
       }
-      // block: lane w of every warp aligns warp w's sum to the row's largest
-      // exponent, and a butterfly over the first NW lanes adds them (integer
-      // sums: the order does not matter)
-      static_assert((NW & (NW - 1)) == 0 && NW <= 32, "power-of-two warp count");
-      const int ew_l = lane < NW ? (int)red_e[(it & 1) * NW + lane] : 1;
-      const int eb = (int)__reduce_max_sync(0xFFFFFFFFu, (uint32_t)ew_l);
+      int eb;
+      uint32_t bbits;
+      U128 tot = block_sum128<NW>(red_s + (it & 1) * NW, red_e + (it & 1) * NW, lane, eb, bbits);
       const bool row_finite = eb < 255;
-      U128 tot = {0ull, 0ull};
-      if (lane < NW) tot = shr128(red_s[(it & 1) * NW + lane], 2 * (eb - ew_l));
-#pragma unroll
-      for (int o = NW / 2; o > 0; o >>= 1) {
-        U128 other;
-        other.hi = __shfl_xor_sync(0xFFFFFFFFu, tot.hi, o);
-        other.lo = __shfl_xor_sync(0xFFFFFFFFu, tot.lo, o);
-        tot = add128(tot, other);
+      // S32 = RN(S), S the exact sum.  With fast sums in the total T, S lies
+      // within 2^-32.6 S of T (every thread's error is below 2^-32.6 U and
+      // its U is at most its largest square, so those bounds add up to at
+      // most 2^-32.6 S; dropped bits below the unit are under 2^-90 S), so
+      // if T - B and T + B round alike for B = 2^-32 T + 1 that is RN(S).
+      // Otherwise (a midpoint within B of T: about 2^-8 of random rows)
+      // every thread forms its exact sum and the block adds them again.
+      // Every warp computes the same T, so the choice is the same in all.
+      float s32 = 0.0f;
+      bool redo = false;
+      if (row_finite && lane == 0) {
+        const int u = 2 * eb - 362;
+        if (bbits & kFastBit) {
+          const U128 bnd = add128(shr128(tot, 32), U128{0ull, 1ull});
+          const float lo_f = u128_scaled_to_f32(sub128(tot, bnd), u, false);
+          const float hi_f = u128_scaled_to_f32(add128(tot, bnd), u, false);
+          redo = __float_as_uint(lo_f) != __float_as_uint(hi_f);
+          s32 = lo_f;
+        } else {
+          s32 = u128_scaled_to_f32(tot, u, (bbits & kStickyBit) != 0u);
+        }
       }
-      // r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))), S the exact sum rounded
-      // once to binary32, every step one IEEE binary32 operation
+      if (__shfl_sync(0xFFFFFFFFu, redo ? 1 : 0, 0)) {
+        // the other exchange slot: its last readers (the previous row) are
+        // past this row's first barrier, and the next row writes it only
+        // after this row's second barrier
+        sticky = false;
+        acc = {0ull, 0ull};
+        if (et < 255) acc = exact_sum_squares<BF16, VPT * E>(&p[0][0], et, sticky);
+        acc = warp_sum128(acc, et, ew, sticky);
+        const bool wst = __any_sync(0xFFFFFFFFu, sticky);
+        const int slot = ((it + 1) & 1) * NW;
+        if (lane == 0) {
+          red_s[slot + warp] = acc;
+          red_e[slot + warp] = (uint32_t)ew | (wst ? kStickyBit : 0u);
+        }
+        __syncthreads();
+        tot = block_sum128<NW>(red_s + slot, red_e + slot, lane, eb, bbits);
+        if (lane == 0) s32 = u128_scaled_to_f32(tot, 2 * eb - 362, (bbits & kStickyBit) != 0u);
+      }
+      // r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))), every step one IEEE
+      // binary32 operation
       float rn32 = 0.0f;
       if (row_finite && lane == 0) {
-        const float s32 = u128_scaled_to_f32(tot, 2 * eb - 362);
         const float ms = __fadd_rn(__fdiv_rn(s32, (float)cin), eps);
         rn32 = __fdiv_rn(1.0f, __fsqrt_rn(ms));
       }
@@ -347,8 +502,9 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 1 : 0) k_quant_act(const uint8
           mul2_rn(p[i][e], p[i][e + 1], sv[e], sv[e + 1]);
         }
 #pragma unroll
-        for (int e = 0; e < E; ++e) m = absmax_nan(m, row_finite ? p[i][e] : __int_as_float(0x7FFFFFFF));
+        for (int e = 0; e < E; ++e) m = absmax_nan(m, p[i][e]);
       }
+      if (!row_finite) m = __int_as_float(0x7FFFFFFF);  // the row's scale is NaN
       const uint32_t mbx = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
       if (lane == 0) red[(it & 1) * NW + warp] = mbx;
       __syncthreads();
