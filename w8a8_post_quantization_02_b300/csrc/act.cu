@@ -290,7 +290,12 @@ SQ_DEVINL U128 block_sum128(const U128* red_s, const uint32_t* red_e, int lane, 
 // NT threads per CTA, each owning VPT 16-byte vectors of every row (vector
 // v = tid + i*NT).  With NT <= 512 the thread's s^-1 values stay in
 // registers; with 1024 threads (rows longer than 32 KiB) the register
-// budget is 64 per thread, so they are re-read through L1 for each row.
+// budget is 64 per thread, so they are re-read through L1 for each row, and
+// so are the RMS-normalizing mode's gains in its 256- and 512-thread blocks:
+// that leaves 62 registers, four 256-thread or two 512-thread blocks per SM
+// instead of two or one (B300: 8192 x 8192 104 -> 94 us, 2048 x 11008
+// 55 -> 47 us, 4096 x 16384 113 -> 100 us; the 128-thread block, already
+// at its four blocks per SM, kept its registers).
 // MODE kStatic: one calibrated scale *d_static for every token instead of
 // the row maximum (no reduction; the clamp can act and `clipped` counts it).
 // MODE kNorm: `s_inv` holds the folded gain gamma' and the row is first
@@ -302,13 +307,14 @@ SQ_DEVINL U128 block_sum128(const U128* red_s, const uint32_t* red_e, int lane, 
 // X' = RN(RN(h * r) * gamma').  Two block barriers per row (three when the
 // exact sum is redone).
 // From 512 threads up the kernel is built for one block per SM, which leaves
-// the compiler its full register budget (0 below: no minimum).  Measured on
+// the compiler its full register budget (0 below: no minimum; the
+// RMS-normalizing mode's 512-thread block for two, see above).  Measured on
 // B300: 2048 x 11008 bf16 24.7 -> 22.4 us (RMS-normalizing mode 70.2 ->
 // 62.0), 4096 x 16384 55.4 -> 45.1 us (175 -> 146); with the same bound on
 // the 256-thread block of 8192-element rows the RMS-normalizing mode lost
 // 4 %, so it applies to the larger blocks only.
 template <bool BF16, int CODES, int NT, int VPT, int MODE>
-__global__ void __launch_bounds__(NT, NT >= 512 ? 1 : 0) k_quant_act(const uint8_t* __restrict__ x, int64_t tokens,
+__global__ void __launch_bounds__(NT, (MODE == kNorm && NT == 512) ? 2 : (NT >= 512 ? 1 : 0)) k_quant_act(const uint8_t* __restrict__ x, int64_t tokens,
                                                   int nvec, int64_t ldx_bytes,
                                                   const float* __restrict__ s_inv,
                                                   uint8_t* __restrict__ xq,
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 1 : 0) k_quant_act(const uint8
   constexpr int E = BF16 ? 8 : 4;
   constexpr int NW = NT / 32;
   constexpr int CB = CODES == SQ_CODES_BF16 ? 2 : 1;
-  constexpr bool kSiReg = NT <= 512;
+  constexpr bool kSiReg = NT <= 512 && !(NORM && NT >= 256);
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t row_bytes = (uint32_t)nvec * 16u;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * row_bytes);
