@@ -287,6 +287,13 @@ SQ_DEVINL U128 block_sum128(const U128* red_s, const uint32_t* red_e, int lane, 
   return tot;
 }
 
+// r = RN(1 / RN(sqrt(RN(RN(s / K) + eps)))), every step one IEEE binary32
+// operation.
+SQ_DEVINL float rms_factor(float s, int K, float eps) {
+  const float ms = __fadd_rn(__fdiv_rn(s, (float)K), eps);
+  return __fdiv_rn(1.0f, __fsqrt_rn(ms));
+}
+
 // NT threads per CTA, each owning VPT 16-byte vectors of every row (vector
 // v = tid + i*NT).  With NT <= 512 the thread's s^-1 values stay in
 // registers; with 1024 threads (rows longer than 32 KiB) the register
@@ -304,7 +311,7 @@ SQ_DEVINL U128 block_sum128(const U128* red_s, const uint32_t* red_e, int lane, 
 // floating-point pipe whose error bound decides the rounding, and redo the
 // exact sum in the rare rows where it cannot), then
 // r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))) in IEEE binary32 and
-// X' = RN(RN(h * r) * gamma').  Two block barriers per row (three when the
+// X' = RN(RN(h * r) * gamma').  Three block barriers per row (five when the
 // exact sum is redone).
 // From 512 threads up the kernel is built for one block per SM, which leaves
 // the compiler its full register budget (0 below: no minimum; the
@@ -439,10 +446,10 @@ __global__ void __launch_bounds__(NT, (MODE == kNorm && NT == 512) ? 2 : (NT >= 
           bulk_g2s_hint(const_cast<uint8_t*>(buf), x + rn * ldx_bytes, row_bytes, &full[stage], pol);
         }
       }
-      int eb;
-      uint32_t bbits;
-      U128 tot = block_sum128<NW>(red_s + (it & 1) * NW, red_e + (it & 1) * NW, lane, eb, bbits);
-      const bool row_finite = eb < 255;
+      // Warp 0 alone forms the row's factor r (the block's total, the bound
+      // check and the scalar chain); the other warps wait for it at a
+      // barrier instead of repeating that work.
+      //
       // S32 = RN(S), S the exact sum.  With fast sums in the total T, S lies
       // within 2^-32.6 S of T (every thread's error is below 2^-32.6 U and
       // its U is at most its largest square, so those bounds add up to at
@@ -450,25 +457,41 @@ __global__ void __launch_bounds__(NT, (MODE == kNorm && NT == 512) ? 2 : (NT >= 
       // if T - B and T + B round alike for B = 2^-32 T + 1 that is RN(S).
       // Otherwise (a midpoint within B of T: about 2^-8 of random rows)
       // every thread forms its exact sum and the block adds them again.
-      // Every warp computes the same T, so the choice is the same in all.
-      float s32 = 0.0f;
-      bool redo = false;
-      if (row_finite && lane == 0) {
-        const int u = 2 * eb - 362;
-        if (bbits & kFastBit) {
-          const U128 bnd = add128(shr128(tot, 32), U128{0ull, 1ull});
-          const float lo_f = u128_scaled_to_f32(sub128(tot, bnd), u, false);
-          const float hi_f = u128_scaled_to_f32(add128(tot, bnd), u, false);
-          redo = __float_as_uint(lo_f) != __float_as_uint(hi_f);
-          s32 = lo_f;
-        } else {
-          s32 = u128_scaled_to_f32(tot, u, (bbits & kStickyBit) != 0u);
+      // r = RN(1 / RN(sqrt(RN(RN(S32 / K) + eps)))), every step one IEEE
+      // binary32 operation.
+      float* rn_s = reinterpret_cast<float*>(red_s + 2 * NW);  // [2]
+      uint32_t* st_s = reinterpret_cast<uint32_t*>(rn_s + 2);   // [2]: 1 redo, 2 finite
+      if (warp == 0) {
+        int eb;
+        uint32_t bbits;
+        const U128 tot = block_sum128<NW>(red_s + (it & 1) * NW, red_e + (it & 1) * NW, lane, eb, bbits);
+        if (lane == 0) {
+          const bool finite = eb < 255;
+          bool redo = false;
+          float s32 = 0.0f;
+          if (finite) {
+            const int u = 2 * eb - 362;
+            if (bbits & kFastBit) {
+              const U128 bnd = add128(shr128(tot, 32), U128{0ull, 1ull});
+              const float lo_f = u128_scaled_to_f32(sub128(tot, bnd), u, false);
+              const float hi_f = u128_scaled_to_f32(add128(tot, bnd), u, false);
+              redo = __float_as_uint(lo_f) != __float_as_uint(hi_f);
+              s32 = lo_f;
+            } else {
+              s32 = u128_scaled_to_f32(tot, u, (bbits & kStickyBit) != 0u);
+            }
+          }
+          if (finite && !redo) rn_s[it & 1] = rms_factor(s32, cin, eps);
+          st_s[it & 1] = (redo ? 1u : 0u) | (finite ? 2u : 0u);
         }
       }
-      if (__shfl_sync(0xFFFFFFFFu, redo ? 1 : 0, 0)) {
-        // the other exchange slot: its last readers (the previous row) are
-        // past this row's first barrier, and the next row writes it only
-        // after this row's second barrier
+      __syncthreads();
+      const uint32_t st = st_s[it & 1];
+      const bool row_finite = (st & 2u) != 0u;
+      if (st & 1u) {
+        // the other exchange slot: its last readers (the previous row's warp
+        // 0) are past this row's first barrier, and the next row writes it
+        // only after this row's last barrier
         sticky = false;
         acc = {0ull, 0ull};
         if (et < 255) acc = exact_sum_squares<BF16, VPT * E>(&p[0][0], et, sticky);
@@ -480,17 +503,16 @@ __global__ void __launch_bounds__(NT, (MODE == kNorm && NT == 512) ? 2 : (NT >= 
           red_e[slot + warp] = (uint32_t)ew | (wst ? kStickyBit : 0u);
         }
         __syncthreads();
-        tot = block_sum128<NW>(red_s + slot, red_e + slot, lane, eb, bbits);
-        if (lane == 0) s32 = u128_scaled_to_f32(tot, 2 * eb - 362, (bbits & kStickyBit) != 0u);
+        if (warp == 0) {
+          int eb;
+          uint32_t bbits;
+          const U128 tot = block_sum128<NW>(red_s + slot, red_e + slot, lane, eb, bbits);
+          if (lane == 0)
+            rn_s[it & 1] = rms_factor(u128_scaled_to_f32(tot, 2 * eb - 362, (bbits & kStickyBit) != 0u), cin, eps);
+        }
+        __syncthreads();
       }
-      // r = RN(1 / RN(sqrt(RN(RN(S / K) + eps)))), every step one IEEE
-      // binary32 operation
-      float rn32 = 0.0f;
-      if (row_finite && lane == 0) {
-        const float ms = __fadd_rn(__fdiv_rn(s32, (float)cin), eps);
-        rn32 = __fdiv_rn(1.0f, __fsqrt_rn(ms));
-      }
-      rn32 = __shfl_sync(0xFFFFFFFFu, rn32, 0);
+      const float rn32 = row_finite ? rn_s[it & 1] : 0.0f;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = tid + i * NT;
@@ -686,7 +708,7 @@ sq_status launch_act(int nvec, const uint8_t* x, int64_t tokens, int64_t ldx_byt
   // the RMS-normalizing mode 24.8 instead of 27.7 us (2048 x 4096).
   const size_t in_flight = 32768;
   const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, in_flight / row_bytes));
-  const size_t smem = stages * row_bytes + kMaxStages * 8 + 2 * (NT / 32) * (4 + 4 + 16) + 16;
+  const size_t smem = stages * row_bytes + kMaxStages * 8 + 2 * (NT / 32) * (4 + 4 + 16) + 16 + 16;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NT, smem) != cudaSuccess)
     return SQ_ERR_CUDA;
