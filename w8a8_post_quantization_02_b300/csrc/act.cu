@@ -289,9 +289,12 @@ SQ_DEVINL U128 block_sum128(const U128* red_s, const uint32_t* red_e, int lane, 
 
 // r = RN(1 / RN(sqrt(RN(RN(s / K) + eps)))), every step one IEEE binary32
 // operation.
+// For K = 2^k, RN(s / K) is RN(s * 2^-k): both round the same real number
+// once.
 SQ_DEVINL float rms_factor(float s, int K, float eps) {
-  const float ms = __fadd_rn(__fdiv_rn(s, (float)K), eps);
-  return __fdiv_rn(1.0f, __fsqrt_rn(ms));
+  const float q = (K & (K - 1)) == 0 ? __fmul_rn(s, __uint_as_float((uint32_t)(127 - (31 - __clz(K))) << 23))
+                                     : __fdiv_rn(s, (float)K);
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(q, eps)));
 }
 
 // NT threads per CTA, each owning VPT 16-byte vectors of every row (vector
@@ -465,23 +468,20 @@ __global__ void __launch_bounds__(NT, (MODE == kNorm && NT == 512) ? 2 : (NT >= 
         int eb;
         uint32_t bbits;
         const U128 tot = block_sum128<NW>(red_s + (it & 1) * NW, red_e + (it & 1) * NW, lane, eb, bbits);
+        // lanes 0 and 1 round T - B and T + B side by side (T alone, with
+        // the sticky bit, when every thread summed exactly)
+        const bool finite = eb < 255;
+        const bool fast_row = (bbits & kFastBit) != 0u;
+        float f = 0.0f;
+        if (finite && lane < 2) {
+          const U128 bnd = add128(shr128(tot, 32), U128{0ull, 1ull});
+          f = !fast_row ? u128_scaled_to_f32(tot, 2 * eb - 362, (bbits & kStickyBit) != 0u)
+                        : u128_scaled_to_f32(lane == 0 ? sub128(tot, bnd) : add128(tot, bnd), 2 * eb - 362, false);
+        }
+        const float f1 = __shfl_sync(0xFFFFFFFFu, f, 1);
         if (lane == 0) {
-          const bool finite = eb < 255;
-          bool redo = false;
-          float s32 = 0.0f;
-          if (finite) {
-            const int u = 2 * eb - 362;
-            if (bbits & kFastBit) {
-              const U128 bnd = add128(shr128(tot, 32), U128{0ull, 1ull});
-              const float lo_f = u128_scaled_to_f32(sub128(tot, bnd), u, false);
-              const float hi_f = u128_scaled_to_f32(add128(tot, bnd), u, false);
-              redo = __float_as_uint(lo_f) != __float_as_uint(hi_f);
-              s32 = lo_f;
-            } else {
-              s32 = u128_scaled_to_f32(tot, u, (bbits & kStickyBit) != 0u);
-            }
-          }
-          if (finite && !redo) rn_s[it & 1] = rms_factor(s32, cin, eps);
+          const bool redo = finite && fast_row && __float_as_uint(f) != __float_as_uint(f1);
+          if (finite && !redo) rn_s[it & 1] = rms_factor(f, cin, eps);
           st_s[it & 1] = (redo ? 1u : 0u) | (finite ? 2u : 0u);
         }
       }
