@@ -13,8 +13,8 @@ flushed before it, for its HBM fraction.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead, on a bounded sample of the same workload.  Under torchrun each rank
-runs an independent replica (the path needs no exchange between ranks in
-this build); the reported time is the max over ranks.
+runs an independent replica (the one-layer path has no exchange between
+ranks); the reported time is the max over ranks.
 """
 from __future__ import annotations
 

@@ -58,7 +58,7 @@ typedef enum {
   SQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, alignment or enum */
   SQ_ERR_NONFINITE = 2,    /* the device word reports a NaN/Inf statistic or scale */
   SQ_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
-  SQ_ERR_UNSUPPORTED = 4,  /* valid request this build does not implement */
+  SQ_ERR_UNSUPPORTED = 4,  /* valid request the library does not implement */
   SQ_ERR_WORKSPACE = 5,    /* workspace pointer missing or too small */
   SQ_ERR_TIMEOUT = 6       /* the device word reports a bounded wait that ran out */
 } sq_status;

@@ -275,7 +275,7 @@ class Layer:
 
 
 def available_codes():
-    """Code formats whose GEMM path this build runs."""
+    """Code formats the library's GEMM runs."""
     return ["i8", "bf16"]
 
 
