@@ -558,6 +558,26 @@ def test_sum_of_squares_rounds_the_exact_sum():
     assert O.sum_squares_f32(np.array([3.0, -4.0], F32)) == F32(25.0)
 
 
+def test_sum_of_squares_sees_terms_below_float64():
+    """A square far below float64's reach still decides a tie: 1 + 2^-24 +
+    2^-120 (and with the tiny element negative, or several of them) rounds
+    up to 1 + 2^-23, while subnormal squares that flush to nothing in binary32
+    (2^-130 squared) also count; just below the tie (1 + 2^-24 - 2^-46 +
+    2^-70, from 2^-12 (1 - 2^-23) in place of 2^-12) rounds down.  Checked
+    against the exact rational sum."""
+    from fractions import Fraction
+    up = F32(1.0 + 2.0 ** -23)
+    for tail in ([2.0 ** -60], [-(2.0 ** -60)], [2.0 ** -70] * 5, [2.0 ** -130], [2.0 ** -149]):
+        row = np.array([1.0, 2.0 ** -12] + tail, F32)
+        exact = sum(Fraction(float(v)) ** 2 for v in row)
+        assert exact > Fraction(1) + Fraction(1, 2 ** 24)
+        assert O.sum_squares_f32(row) == up
+    below = np.array([1.0, 2.0 ** -12 * (1.0 - 2.0 ** -23)], F32)
+    exact = sum(Fraction(float(v)) ** 2 for v in below)
+    assert Fraction(1) < exact < Fraction(1) + Fraction(1, 2 ** 24)
+    assert O.sum_squares_f32(below) == F32(1.0)
+
+
 def test_folded_gain_matches_unfolded_path():
     """Folding S^-1 into the gain changes only roundings: X' from the fold
     is within 2 fp32 ulps of RMSNorm-then-X*S^-1, and in exact arithmetic
