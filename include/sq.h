@@ -250,9 +250,8 @@ sq_status sq_quant_act_static(const void* x, sq_dtype dt, int64_t tokens, int64_
  *   S_t = the exact sum_j h[t,j]^2, rounded once to binary32 (parts of
  *         squares below 2^-108 of the largest square among the (at most
  *         32) values one thread sums enter only as a sticky bit, so only a
- *         row built to lie
- *         within 2^-98 of a binary32 midpoint through several such parts
- *         can round the other way)
+ *         row built to lie within 2^-98 of a binary32 midpoint through
+ *         several such parts can round the other way)
  *   r_t = RN(1 / RN(sqrt(RN(RN(S_t / cin) + eps))))   (IEEE binary32 steps)
  *   X'[t,j] = RN(RN(h[t,j] * r_t) * gamma_folded[j])
  * followed by the dynamic per-token quantizer of sq_quant_act (same codes,
